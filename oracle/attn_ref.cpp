@@ -1,0 +1,361 @@
+// fp64 CPU oracle for the fused exact-attention forward and its FP8 prep.
+//
+// TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+// benchmark's CPU-baseline leg load this library.  It shares no code, header
+// or constant table with the CUDA path, and the CUDA path never calls it.
+//
+// Sources (the pages the method is described on):
+//  [R] "深度解读报告：FlashAttention-3（2024）" (FlashAttention-3 deep-reading
+//      report): §3 intro (tiling with running max m and running sum l, the
+//      N x N matrix never written to HBM), §2.2 and §3.3 (block quantization,
+//      incoherent processing M = diag(+-1) x Hadamard with M M^T = I),
+//      §4.3 (errors are measured against an FP64 reference implementation).
+//  [E] "Efficient Attention & FlashAttention: 解释 FlashAttention-2/3 的改进",
+//      "数学机理" (FA2 normalises once per query block; the result is still
+//      the plain softmax attention).
+//
+// What is computed.  The tiled, online-softmax method reaches exactly (up to
+// rounding order) the plain definition of attention, so the oracle is that
+// definition, written out in double precision with every score of a row
+// materialised and a two-pass softmax:
+//     s_j   = scale * sum_c q_ic k_jc           for every visible key j
+//     m     = max_j s_j
+//     l     = sum_j exp(s_j - m)
+//     O_i   = sum_j exp(s_j - m) v_j / l
+//     LSE_i = m + log(l)                        (natural log)
+// Visibility of key j to query i: j <= i when causal; j > i - window when
+// window > 0.  A row that sees no key gets O = 0 and LSE = -inf.
+//
+// FP8 prep (block quantization + incoherent processing, [R] §2.2 / §3.3):
+//     r   = x M  with M = D H_d / sqrt(d)   (Q and K; V is not rotated)
+//     per block of `block_rows` consecutive tokens of one (batch, head):
+//         amax  = max |r|           scale = amax / 448  (1 when amax == 0)
+//         code  = e4m3(r / scale)   (round to nearest even, saturate to 448)
+// The rotation is a dense d x d product in double.  The quantisation decision
+// (amax, scale, r / scale and the rounding to e4m3) is taken in binary32,
+// the precision the CUDA path takes it in, so that a code is comparable bit
+// for bit.  The OCP 8-bit floating point specification (OFP8, E4M3: 1 sign,
+// 4 exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is
+// NaN, largest finite 448) defines the encoder below.
+//
+// Random signs of D: bit 63 of successive outputs of splitmix64 seeded with
+// the caller's seed (Steele, Lea and Flood 2014; Vigna's public reference
+// splitmix64.c): output c (c = 0, 1, ...) is mix(seed + (c + 1) * gamma).
+// A set bit gives -1.
+//
+// Portable C++17; no intrinsics, runs the same on x86-64 and aarch64.
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+#include <thread>
+#include <vector>
+
+namespace {
+
+double bf16_value(uint16_t bits) {
+    uint32_t u = static_cast<uint32_t>(bits) << 16;
+    float f;
+    std::memcpy(&f, &u, sizeof f);
+    return static_cast<double>(f);
+}
+
+bool key_visible(long i, long j, int causal, int window) {
+    if (causal && j > i) return false;
+    if (window > 0 && j <= i - window) return false;
+    return true;
+}
+
+int pick_threads(int requested, long work_items) {
+    int t = requested > 0 ? requested : static_cast<int>(std::thread::hardware_concurrency());
+    if (t < 1) t = 1;
+    if (work_items < t) t = static_cast<int>(std::max<long>(1, work_items));
+    return t;
+}
+
+template <class F>
+void parallel_for(long count, int nthreads, F&& body) {
+    int t = pick_threads(nthreads, count);
+    if (t == 1) {
+        for (long i = 0; i < count; ++i) body(i);
+        return;
+    }
+    std::atomic<long> next{0};
+    std::vector<std::thread> pool;
+    pool.reserve(t);
+    for (int w = 0; w < t; ++w) {
+        pool.emplace_back([&] {
+            for (long i = next.fetch_add(1); i < count; i = next.fetch_add(1)) body(i);
+        });
+    }
+    for (auto& th : pool) th.join();
+}
+
+// One query row of one (batch, head): the plain two-pass definition.
+// in(b, n, h, c) reads element c of token n, head h of batch b from a
+// (B, N, H, d) tensor.  probs (optional) receives the N softmax weights.
+template <class In>
+void attention_row(const In& qin, const In& kin, const In& vin, long b, long h, long i,
+                   long N, long d, int causal, double scale, int window,
+                   double* o_row, double* lse_out, double* probs) {
+    std::vector<double> s(N, -std::numeric_limits<double>::infinity());
+    std::vector<double> q(d);
+    for (long c = 0; c < d; ++c) q[c] = qin(b, i, h, c);
+    double m = -std::numeric_limits<double>::infinity();
+    bool any = false;
+    for (long j = 0; j < N; ++j) {
+        if (!key_visible(i, j, causal, window)) continue;
+        double acc = 0.0;
+        for (long c = 0; c < d; ++c) acc += q[c] * kin(b, j, h, c);
+        s[j] = scale * acc;
+        if (!any || s[j] > m) m = s[j];
+        any = true;
+    }
+    for (long c = 0; c < d; ++c) o_row[c] = 0.0;
+    if (!any) {
+        *lse_out = -std::numeric_limits<double>::infinity();
+        if (probs) for (long j = 0; j < N; ++j) probs[j] = 0.0;
+        return;
+    }
+    double l = 0.0;
+    for (long j = 0; j < N; ++j) {
+        if (!key_visible(i, j, causal, window)) { s[j] = 0.0; continue; }
+        s[j] = std::exp(s[j] - m);
+        l += s[j];
+    }
+    for (long j = 0; j < N; ++j) {
+        if (!key_visible(i, j, causal, window)) continue;
+        const double w = s[j];
+        for (long c = 0; c < d; ++c) o_row[c] += w * vin(b, j, h, c);
+    }
+    for (long c = 0; c < d; ++c) o_row[c] /= l;
+    *lse_out = m + std::log(l);
+    if (probs) {
+        for (long j = 0; j < N; ++j) probs[j] = key_visible(i, j, causal, window) ? s[j] / l : 0.0;
+    }
+}
+
+struct Bf16Tensor {
+    const uint16_t* p; long N, H, d;
+    double operator()(long b, long n, long h, long c) const { return bf16_value(p[((b * N + n) * H + h) * d + c]); }
+};
+struct F64Tensor {
+    const double* p; long N, H, d;
+    double operator()(long b, long n, long h, long c) const { return p[((b * N + n) * H + h) * d + c]; }
+};
+
+// Output layout: o is (B, H, R, d) and lse is (B, H, R), R = number of rows
+// computed (all N rows when rows == nullptr).
+template <class In>
+int run_attention(const In& q, const In& k, const In& v, double* o, double* lse,
+                  int B, int H, int N, int d, int causal, double scale, int window,
+                  const int* rows, int nrows, int nthreads) {
+    if (B < 0 || H < 0 || N < 0 || d <= 0) return -1;
+    const long R = rows ? nrows : N;
+    for (long r = 0; rows && r < R; ++r) if (rows[r] < 0 || rows[r] >= N) return -1;
+    const long items = static_cast<long>(B) * H * R;
+    parallel_for(items, nthreads, [&](long it) {
+        const long r = it % R;
+        const long bh = it / R;
+        const long b = bh / H, h = bh % H;
+        const long i = rows ? rows[r] : r;
+        attention_row(q, k, v, b, h, i, N, d, causal, scale, window,
+                      o + it * d, lse + it, nullptr);
+    });
+    return 0;
+}
+
+// ---- OCP FP8 E4M3 --------------------------------------------------------
+
+double e4m3_decode_one(uint8_t code) {
+    const int sign = code >> 7;
+    const int e = (code >> 3) & 0xF;
+    const int m = code & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return std::numeric_limits<double>::quiet_NaN();
+    if (e == 0) v = std::ldexp(static_cast<double>(m), -9);          // m/8 * 2^-6
+    else v = std::ldexp(8.0 + m, e - 7 - 3);                          // (1 + m/8) * 2^(e-7)
+    return sign ? -v : v;
+}
+
+// Round half to even of a non-negative double that holds at most 53 bits.
+double round_half_even(double x) {
+    double f = std::floor(x);
+    double r = x - f;
+    if (r > 0.5) return f + 1.0;
+    if (r < 0.5) return f;
+    return (std::fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+// Encode with round-to-nearest-even and saturation to the largest finite
+// magnitude (448); NaN encodes as 0x7F with the sign bit of the input.
+uint8_t e4m3_encode_one(double x) {
+    const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+    if (std::isnan(x)) return static_cast<uint8_t>(sign | 0x7F);
+    double a = std::fabs(x);
+    if (a >= 448.0) return static_cast<uint8_t>(sign | 0x7E);
+    const double min_normal = std::ldexp(1.0, -6);
+    if (a < min_normal) {
+        // Subnormal grid: multiples of 2^-9 (exact scaling by a power of two).
+        double n = round_half_even(std::ldexp(a, 9));
+        if (n >= 8.0) return static_cast<uint8_t>(sign | (1 << 3));  // rounds up to 2^-6
+        return static_cast<uint8_t>(sign | static_cast<int>(n));
+    }
+    int e2;
+    std::frexp(a, &e2);            // a = f * 2^e2, f in [0.5, 1)
+    int e = e2 - 1;                // a in [2^e, 2^(e+1))
+    double n = round_half_even(std::ldexp(a, 3 - e));  // 8 <= n <= 16
+    if (n >= 16.0) { n = 8.0; e += 1; }
+    double val = std::ldexp(n, e - 3);
+    if (val > 448.0) return static_cast<uint8_t>(sign | 0x7E);
+    const int ef = e + 7;
+    const int mf = static_cast<int>(n) - 8;
+    return static_cast<uint8_t>(sign | (ef << 3) | mf);
+}
+
+// ---- splitmix64 signs and the Hadamard rotation --------------------------
+
+uint64_t splitmix64_output(uint64_t seed, uint64_t c) {
+    uint64_t z = seed + (c + 1) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+double sign_of(uint64_t seed, long c) { return (splitmix64_output(seed, c) >> 63) ? -1.0 : 1.0; }
+
+// Sylvester ordering: H[r][c] = (-1)^popcount(r & c).
+double sylvester(long r, long c) {
+    unsigned long x = static_cast<unsigned long>(r & c);
+    int parity = 0;
+    while (x) { parity ^= 1; x &= x - 1; }
+    return parity ? -1.0 : 1.0;
+}
+
+bool is_pow2(long d) { return d > 0 && (d & (d - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int oracle_attn_fwd_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         double* o, double* lse, int B, int H, int N, int d,
+                         int causal, double scale, int window,
+                         const int* rows, int nrows, int nthreads) {
+    Bf16Tensor Q{q, N, H, d}, K{k, N, H, d}, V{v, N, H, d};
+    return run_attention(Q, K, V, o, lse, B, H, N, d, causal, scale, window, rows, nrows, nthreads);
+}
+
+int oracle_attn_fwd_f64(const double* q, const double* k, const double* v,
+                        double* o, double* lse, int B, int H, int N, int d,
+                        int causal, double scale, int window,
+                        const int* rows, int nrows, int nthreads) {
+    F64Tensor Q{q, N, H, d}, K{k, N, H, d}, V{v, N, H, d};
+    return run_attention(Q, K, V, o, lse, B, H, N, d, causal, scale, window, rows, nrows, nthreads);
+}
+
+// Softmax weights of one query row (length N; zero for hidden keys).
+int oracle_attn_row_probs_f64(const double* q, const double* k, const double* v,
+                              int B, int H, int N, int d, int causal, double scale, int window,
+                              int b, int h, int i, double* probs) {
+    if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= N) return -1;
+    F64Tensor Q{q, N, H, d}, K{k, N, H, d}, V{v, N, H, d};
+    std::vector<double> orow(d);
+    double lse;
+    attention_row(Q, K, V, b, h, i, N, d, causal, scale, window, orow.data(), &lse, probs);
+    return 0;
+}
+
+void oracle_e4m3_encode_f64(const double* x, uint8_t* out, long n) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_encode_one(x[i]);
+}
+
+void oracle_e4m3_decode(const uint8_t* codes, double* out, long n) {
+    for (long i = 0; i < n; ++i) out[i] = e4m3_decode_one(codes[i]);
+}
+
+// M = D H_d / sqrt(d), row-major d x d.
+int oracle_rotation_matrix(int d, unsigned long long seed, double* M) {
+    if (!is_pow2(d)) return -1;
+    const double inv = 1.0 / std::sqrt(static_cast<double>(d));
+    for (long r = 0; r < d; ++r) {
+        const double sr = sign_of(seed, r);
+        for (long c = 0; c < d; ++c) M[r * d + c] = sr * sylvester(r, c) * inv;
+    }
+    return 0;
+}
+
+void oracle_signs(int d, unsigned long long seed, double* out) {
+    for (long c = 0; c < d; ++c) out[c] = sign_of(seed, c);
+}
+
+// x: bf16 (B, N, H, d).  x8: e4m3 codes (B, N, H, d).  scales: float
+// (B, H, ceil(N / block_rows)).  rotated (optional): the binary32 values r
+// that were quantised, (B, N, H, d).
+// mode 0: per-block scales; 1: per-block scales after the rotation (not for
+// V); 2: one scale for the whole tensor (written to every block entry).
+int oracle_fp8_quantize(const uint16_t* x, uint8_t* x8, float* scales, float* rotated,
+                        int B, int H, int N, int d, int block_rows, int mode,
+                        unsigned long long seed, int is_v, int nthreads) {
+    if (B < 0 || H < 0 || N < 0 || d <= 0 || block_rows <= 0 || mode < 0 || mode > 2) return -1;
+    const bool rotate = (mode == 1) && !is_v;
+    if (rotate && !is_pow2(d)) return -1;
+    const long nblk = (N + block_rows - 1) / block_rows;
+    const long total = static_cast<long>(B) * N * H * d;
+    std::vector<float> r(total);
+    std::vector<double> M;
+    if (rotate) {
+        M.resize(static_cast<size_t>(d) * d);
+        oracle_rotation_matrix(d, seed, M.data());
+    }
+    // r = x M (double sum, rounded once to binary32) or r = x.
+    parallel_for(static_cast<long>(B) * N * H, nthreads, [&](long row) {
+        const uint16_t* xr = x + row * d;
+        float* rr = r.data() + row * d;
+        if (!rotate) {
+            for (long c = 0; c < d; ++c) rr[c] = static_cast<float>(bf16_value(xr[c]));
+            return;
+        }
+        for (long c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (long t = 0; t < d; ++t) acc += bf16_value(xr[t]) * M[t * d + c];
+            rr[c] = static_cast<float>(acc);
+        }
+    });
+    auto at = [&](long b, long n, long h, long c) -> float& {
+        return r[((b * N + n) * H + h) * d + c];
+    };
+    // Block amax (binary32 magnitudes; the maximum is exact).
+    std::vector<float> amax(static_cast<size_t>(B) * H * nblk, 0.0f);
+    parallel_for(static_cast<long>(B) * H * nblk, nthreads, [&](long it) {
+        const long blk = it % nblk, bh = it / nblk, b = bh / H, h = bh % H;
+        float a = 0.0f;
+        for (long n = blk * block_rows; n < std::min<long>(N, (blk + 1) * block_rows); ++n)
+            for (long c = 0; c < d; ++c) a = std::max(a, std::fabs(at(b, n, h, c)));
+        amax[it] = a;
+    });
+    if (mode == 2) {
+        float a = 0.0f;
+        for (float v : amax) a = std::max(a, v);
+        std::fill(amax.begin(), amax.end(), a);
+    }
+    for (size_t i = 0; i < amax.size(); ++i) {
+        const float a = amax[i];
+        scales[i] = (a > 0.0f) ? a / 448.0f : 1.0f;      // binary32 division
+    }
+    parallel_for(static_cast<long>(B) * N * H, nthreads, [&](long row) {
+        const long h = row % H, bn = row / H, n = bn % N, b = bn / N;
+        const float s = scales[(b * H + h) * nblk + n / block_rows];
+        for (long c = 0; c < d; ++c) {
+            const float y = r[row * d + c] / s;              // binary32 division
+            x8[row * d + c] = e4m3_encode_one(static_cast<double>(y));
+        }
+    });
+    if (rotated) std::memcpy(rotated, r.data(), sizeof(float) * total);
+    return 0;
+}
+
+}  // extern "C"
