@@ -1,0 +1,192 @@
+"""ctypes binding of libattn_sm103.so (argument marshalling only).
+
+Every step of the attention path runs in the library's CUDA kernels; torch
+is used here for device memory, streams and the tensor objects that carry
+the pointers.  There is no fallback: if the library is missing or cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn_sm103.so")
+
+MODE_BLOCK, MODE_BLOCK_HADAMARD, MODE_PER_TENSOR = 0, 1, 2
+BLOCK_ROWS = 128
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A call into the attention library returned an error status."""
+
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed ({code}): {msg}")
+        self.code = code
+
+
+def library() -> ctypes.CDLL:
+    """Load the shared library (built by ``exact_attention_71_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m exact_attention_71_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i, f, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong
+        L.attn_fwd.argtypes = [P, P, P, P, P, i, i, i, i, i, f, i, P]
+        L.attn_fwd.restype = i
+        L.attn_fwd_fp8.argtypes = [P, P, P, P, P, i, i, i, i, i, f, i, P, P, P, P]
+        L.attn_fwd_fp8.restype = i
+        L.attn_fp8_prep.argtypes = [P, P, P, i, i, i, i, i, i, u64, i, P]
+        L.attn_fp8_prep.restype = i
+        L.attn_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
+        L.attn_device_status.restype = i
+        L.attn_set_wait_limit.argtypes = [u64]
+        L.attn_set_wait_limit.restype = i
+        L.attn_last_error_string.argtypes = []
+        L.attn_last_error_string.restype = ctypes.c_char_p
+        _lib = L
+        return _lib
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != 0:
+        msg = library().attn_last_error_string().decode(errors="replace")
+        raise AttnError(fn, rc, msg)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check_qkv(q, k, v, dtype):
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one (batch, seqlen, heads, head_dim) shape")
+    for t in (q, k, v):
+        if t.dtype != dtype:
+            raise ValueError(f"expected dtype {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+
+
+def _outputs(q, out, lse):
+    B, N, H, d = q.shape
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != (B, N, H, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 (B, N, H, d) tensor")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, N) tensor")
+    return out, lse
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0,
+             out=None, lse=None, stream=None):
+    """bf16 fused attention forward.  q, k, v: (B, N, H, d) bf16 CUDA tensors.
+
+    Returns (O (B, N, H, d) bf16, LSE (B, H, N) float32, natural log).
+    """
+    _check_qkv(q, k, v, torch.bfloat16)
+    out, lse = _outputs(q, out, lse)
+    B, N, H, d = q.shape
+    rc = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
+                            float(scale or 0.0), int(window), ctypes.c_void_p(_stream(stream)))
+    _check("attn_fwd", rc)
+    return out, lse
+
+
+def attn_fp8_prep(x, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0, is_v: bool = False,
+                  out=None, scales=None, stream=None):
+    """Rotation (mode 1, not V) + block quantisation of one bf16 (B,N,H,d) tensor.
+
+    Returns (codes as a torch.uint8 (B,N,H,d) tensor, scales float32 (B,H,ceil(N/128))).
+    """
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 4 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 (B, N, H, d) CUDA tensor")
+    B, N, H, d = x.shape
+    nblk = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((B, H, nblk), dtype=torch.float32, device=x.device)
+    rc = library().attn_fp8_prep(_ptr(x), _ptr(out), _ptr(scales), B, H, N, d, BLOCK_ROWS, int(mode),
+                                 int(sign_seed) & 0xFFFFFFFFFFFFFFFF, int(bool(is_v)),
+                                 ctypes.c_void_p(_stream(stream)))
+    _check("attn_fp8_prep", rc)
+    return out, scales
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, scale: float | None = None,
+                 window: int = 0, out=None, lse=None, stream=None):
+    """FP8 e4m3 fused attention forward on codes from attn_fp8_prep.
+
+    q8, k8, v8: uint8 (or float8_e4m3fn) (B, N, H, d) CUDA tensors; *_scale:
+    float32 (B, H, ceil(N/128)).  Returns (O bf16 (B,N,H,d), LSE (B,H,N)).
+    """
+    for t in (q8, k8, v8):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q8, k8, v8 must be contiguous e4m3 codes on the GPU")
+    if q8.dim() != 4 or q8.shape != k8.shape or q8.shape != v8.shape:
+        raise ValueError("q8, k8, v8 must share one (B, N, H, d) shape")
+    B, N, H, d = q8.shape
+    nblk = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
+    for s in (q_scale, k_scale, v_scale):
+        if s.shape != (B, H, nblk) or s.dtype != torch.float32 or not s.is_contiguous():
+            raise ValueError("scales must be contiguous float32 (B, H, ceil(N/128)) tensors")
+    out, lse = _outputs(q8, out, lse)
+    rc = library().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(out), _ptr(lse), B, H, N, d,
+                                int(bool(causal)), float(scale or 0.0), int(window), _ptr(q_scale),
+                                _ptr(k_scale), _ptr(v_scale), ctypes.c_void_p(_stream(stream)))
+    _check("attn_fwd_fp8", rc)
+    return out, lse
+
+
+def fp8_prepare_qkv(q, k, v, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0, stream=None):
+    """Runs the prep on Q, K (rotated in mode 1) and V (never rotated)."""
+    q8, qs = attn_fp8_prep(q, mode, sign_seed, False, stream=stream)
+    k8, ks = attn_fp8_prep(k, mode, sign_seed, False, stream=stream)
+    v8, vs = attn_fp8_prep(v, mode, sign_seed, True, stream=stream)
+    return q8, k8, v8, qs, ks, vs
+
+
+def device_status(stream=None):
+    """(status, site): waits for the stream and reads/clears the status word."""
+    site = ctypes.c_int(0)
+    rc = library().attn_device_status(ctypes.c_void_p(_stream(stream)), ctypes.byref(site))
+    return rc, site.value
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0,
+                  device="cuda", stream=None):
+    """End-to-end call on HOST tensors: copies q, k, v to the device, runs
+    attn_fwd, and copies O and LSE back (pinned host buffers are used as-is)."""
+    dev = torch.device(device)
+    qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
+    o, lse = attn_fwd(qd, kd, vd, causal=causal, scale=scale, window=window, stream=stream)
+    return o.to("cpu"), lse.to("cpu")
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

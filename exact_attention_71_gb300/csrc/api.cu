@@ -1,0 +1,233 @@
+// C ABI of the fused exact-attention forward: argument checks, TMA tensor
+// maps, dispatch to the kernel instantiations, status and error reporting.
+// The declarations and the contract are in include/attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_launch.cuh"
+#include "fp8_prep.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Device status word: first failing wait site of any kernel launched by the
+// library (0 = none).  Its address is looked up once per device.
+__device__ int g_attn_status;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mutex;
+
+constexpr unsigned long long kDefaultWaitLimit = 4000000000ull;   // ~2 s of SM clock
+std::atomic<unsigned long long> g_wait_limit{kDefaultWaitLimit};
+
+int status_ptr(int** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (!g_status_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_attn_status);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        g_status_ptr[dev] = static_cast<int*>(ptr);
+    }
+    *out = g_status_ptr[dev];
+    return ATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// (B, N, H, d) tensor viewed as 4-D {d, H, N, B}; box = one 128-byte column
+// block of `rows` tokens of one head, 128-byte swizzle (the layout the MMA
+// shared-memory descriptors expect).  Rows past N read as zero.
+int make_map(CUtensorMap* map, const void* base, int B, int H, int N, int d, int elem_bytes, int rows) {
+    auto enc = encode_fn();
+    if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const CUtensorMapDataType dt =
+        elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * elem_bytes, static_cast<cuuint64_t>(H) * d * elem_bytes,
+                             static_cast<cuuint64_t>(N) * H * d * elem_bytes};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elem_bytes), 1, static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t estride[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+    return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int N,
+                 int d, int window) {
+    if (B < 0 || H < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d N=%d)", B, H, N);
+    if (d != 64 && d != 128 && d != 256) return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128, 256)", d);
+    if (window < 0) return fail(ATTN_ERR_INVALID_ARG, "window %d < 0", window);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    if (!q || !k || !v || !o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    const long long items = static_cast<long long>(B) * H * ((N + 127) / 128);
+    if (items >= (1ll << 31)) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
+    return ATTN_OK;
+}
+
+float resolve_scale(float scale, int d) {
+    if (!(scale > 0.0f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt(static_cast<float>(d));
+    return scale;
+}
+
+int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                   int d, int causal, float scale, int window, const float* qs, const float* ks, const float* vs,
+                   void* stream) {
+    attn::FwdGeometry g;
+    cudaError_t (*run)(const attn::FwdMaps&, const attn::FwdParams&, cudaStream_t) = nullptr;
+    if (fp8) {
+        if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 only (got %d)", d);
+        g = attn::geom_fp8_d128();
+        run = attn::run_fwd_fp8_d128;
+    } else if (d == 64) {
+        g = attn::geom_bf16_d64();
+        run = attn::run_fwd_bf16_d64;
+    } else if (d == 128) {
+        g = attn::geom_bf16_d128();
+        run = attn::run_fwd_bf16_d128;
+    } else {
+        g = attn::geom_bf16_d256();
+        run = attn::run_fwd_bf16_d256;
+    }
+    attn::FwdMaps maps;
+    int rc;
+    if ((rc = make_map(&maps.q, q, B, H, N, d, g.elem_bytes, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.k, k, B, H, N, d, g.elem_bytes, g.bn)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.v, v, B, H, N, d, g.elem_bytes, g.bn)) != ATTN_OK) return rc;
+    attn::FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.q_scale = qs;
+    p.k_scale = ks;
+    p.v_scale = vs;
+    p.B = B;
+    p.H = H;
+    p.N = N;
+    p.causal = causal ? 1 : 0;
+    p.window = window;
+    p.scale_log2 = resolve_scale(scale, d) * 1.4426950408889634f;
+    p.n_mblocks = (N + g.nq * 128 - 1) / (g.nq * 128);
+    p.wait_limit = g_wait_limit.load();
+    if ((rc = status_ptr(&p.status)) != ATTN_OK) return rc;
+    cudaError_t e = run(maps, p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd launch");
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+             int causal, float scale, int window, void* stream) {
+    g_err[0] = '\0';
+    int rc = check_common(q, k, v, o, lse, B, H, N, d, window);
+    if (rc != ATTN_OK || static_cast<long long>(B) * H * N == 0) return rc;
+    return launch_forward(false, q, k, v, o, lse, B, H, N, d, causal, scale, window, nullptr, nullptr, nullptr,
+                          stream);
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse, int B, int H, int N, int d,
+                 int causal, float scale, int window, const float* q_scale, const float* k_scale,
+                 const float* v_scale, void* stream) {
+    g_err[0] = '\0';
+    int rc = check_common(q8, k8, v8, o, lse, B, H, N, d, window);
+    if (rc != ATTN_OK || static_cast<long long>(B) * H * N == 0) return rc;
+    if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 only (got %d)", d);
+    if (!q_scale || !k_scale || !v_scale) return fail(ATTN_ERR_INVALID_ARG, "null scale pointer");
+    return launch_forward(true, q8, k8, v8, o, lse, B, H, N, d, causal, scale, window, q_scale, k_scale, v_scale,
+                          stream);
+}
+
+int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, int d, int block_rows, int mode,
+                  unsigned long long sign_seed, int is_v, void* stream) {
+    g_err[0] = '\0';
+    if (B < 0 || H < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d N=%d)", B, H, N);
+    if (d != 64 && d != 128 && d != 256) return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128, 256)", d);
+    if (block_rows != 128) return fail(ATTN_ERR_UNSUPPORTED, "block_rows must be 128 (got %d)", block_rows);
+    if (mode < 0 || mode > 2) return fail(ATTN_ERR_INVALID_ARG, "mode %d (0, 1 or 2)", mode);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    if (!x || !x8 || !scales) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(x8) || !aligned16(scales))
+        return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    cudaError_t e = attn::run_fp8_prep(x, x8, scales, B, H, N, d, mode, sign_seed, is_v != 0,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_fp8_prep launch");
+    return ATTN_OK;
+}
+
+int attn_device_status(void* stream, int* site) {
+    g_err[0] = '\0';
+    if (site) *site = 0;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int* ptr = nullptr;
+    int rc = status_ptr(&ptr);
+    if (rc != ATTN_OK) return rc;
+    int value = 0;
+    e = cudaMemcpy(&value, ptr, sizeof value, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+    if (value != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+        if (site) *site = value;
+        return fail(ATTN_ERR_DEVICE_TIMEOUT, "a kernel gave up waiting at site 0x%x", value);
+    }
+    return ATTN_OK;
+}
+
+int attn_set_wait_limit(unsigned long long cycles) {
+    g_err[0] = '\0';
+    g_wait_limit.store(cycles ? cycles : kDefaultWaitLimit);
+    return ATTN_OK;
+}
+
+const char* attn_last_error_string(void) { return g_err; }
+
+}  // extern "C"

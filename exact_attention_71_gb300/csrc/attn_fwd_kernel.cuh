@@ -1,0 +1,534 @@
+// Fused exact-attention forward for sm_103a (bf16 and FP8 e4m3 inputs).
+//
+// Method (FlashAttention-3 deep-reading report, "第三层" intro, §3.1, §3.2,
+// §3.3; "Efficient Attention & FlashAttention", "数学机理"): K and V are
+// streamed tile by tile past a resident tile of queries; every query row keeps
+// a running maximum m and a running sum l of its exponentiated scores; the
+// output accumulator is rescaled whenever m grows and divided by l once at
+// the end.  The N x N score matrix only ever exists one 128 x BN tile at a
+// time, in tensor memory.
+//
+// GB300 mapping (one CTA per SM, warp-specialised):
+//   warps [0, 4*NQ)   softmax warpgroups; warpgroup t owns query tile t
+//                     (128 rows, one thread per row, TMEM lanes = rows)
+//   warp  4*NQ        TMA producer: Q tiles once, then K_j, V_j into an
+//                     NSTAGE-deep shared-memory ring (full/empty mbarriers)
+//   warp  4*NQ+1      MMA issuer: tcgen05.mma S_t = Q_t K_j^T (both operands
+//                     in shared memory) and O_t += P_t V_j (P from tensor
+//                     memory, V from shared memory), completion signalled
+//                     with tcgen05.commit
+// Tensor memory (512 columns x 128 lanes of fp32):
+//   S_t at columns [128 t, 128 t + BN); P_t (bf16 pairs or e4m3 quads)
+//   overwrites the first columns of S_t; O_t at columns [256 + D t, ...).
+// The two query tiles alternate on the tensor pipe: while warpgroup 0 runs
+// the softmax of S_0(j), the pipe computes O_1 += P_1 V_{j-1} and
+// S_1(j) = Q_1 K_j^T (the report's §3.1 ping-pong of softmax against the
+// other tile's GEMMs, with the GEMM of one iteration overlapping the softmax
+// of the next as in §3.2).
+//
+// Every barrier wait is bounded: a role that gives up records a site code in
+// the status word, raises a shared abort flag and leaves its loop, so the CTA
+// always reaches its teardown (TMEM free) instead of hanging.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+struct FwdParams {
+    void* o;                 // bf16 (B, N, H, D)
+    float* lse;              // fp32 (B, H, N)
+    const float* q_scale;    // FP8 only: (B, H, nblk)
+    const float* k_scale;
+    const float* v_scale;
+    int B, H, N;
+    int causal, window;
+    float scale_log2;        // softmax scale * log2(e)
+    int n_mblocks;           // ceil(N / (NQ * 128))
+    unsigned long long wait_limit;
+    int* status;             // device status word (first failing site)
+};
+
+// Status site codes: role * 16 + barrier.
+enum : int {
+    SITE_LOAD_EMPTY = 0x11,
+    SITE_LOAD_DRAIN = 0x12,
+    SITE_MMA_Q = 0x21,
+    SITE_MMA_FULL = 0x22,
+    SITE_MMA_P = 0x23,
+    SITE_MMA_DRAIN = 0x24,
+    SITE_SOFTMAX_S = 0x31,
+    SITE_SOFTMAX_O = 0x32,
+};
+
+template <int D_, int BN_, int NQ_, bool FP8_>
+struct FwdCfg {
+    static constexpr int D = D_;
+    static constexpr int BN = BN_;
+    static constexpr int NQ = NQ_;
+    static constexpr bool FP8 = FP8_;
+    static constexpr int BM = 128;                       // query rows per tile
+    static constexpr int ES = FP8 ? 1 : 2;               // bytes per element
+    static constexpr int ROW_BYTES = D * ES;
+    static constexpr int NCB = ROW_BYTES / 128;          // 128-byte column boxes
+    static constexpr int BOX_ELEMS = 128 / ES;
+    static constexpr int Q_TILE_BYTES = BM * ROW_BYTES;
+    static constexpr int KV_TILE_BYTES = BN * ROW_BYTES;
+    static constexpr int RING_BUDGET = 196 * 1024 - NQ * Q_TILE_BYTES;
+    static constexpr int NSTAGE_RAW = RING_BUDGET / KV_TILE_BYTES;
+    static constexpr int NSTAGE = NSTAGE_RAW > 8 ? 8 : NSTAGE_RAW;
+    static constexpr int MMA_K = FP8 ? 32 : 16;          // K per MMA instruction
+    static constexpr int P_COLS = BN * ES / 4;           // TMEM columns of one P row
+    static constexpr int S_COL = 128;                    // column stride of S_t
+    static constexpr int O_COL0 = 256;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NUM_SOFTMAX_THREADS = NQ * 128;
+    static constexpr int LOAD_WARP = NQ * 4;
+    static constexpr int MMA_WARP = NQ * 4 + 1;
+    static constexpr int THREADS = NQ * 128 + 128;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + NQ * Q_TILE_BYTES + NSTAGE * KV_TILE_BYTES + BAR_BYTES;
+
+    static_assert(D == 64 || D == 128 || D == 256, "head_dim");
+    static_assert(BN == 64 || BN == 128, "key tile");
+    static_assert(NCB >= 1 && ROW_BYTES % 128 == 0, "rows must be whole 128-byte boxes");
+    static_assert(NQ * 128 + 0 <= 256 && O_COL0 + NQ * D <= TMEM_COLS, "tensor memory budget");
+    static_assert(NSTAGE >= 2, "ring depth");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+struct SharedBarriers {
+    uint64_t q_full[2];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_full[2];
+    uint64_t drain;
+    uint64_t ring_full[8];
+    uint64_t ring_empty[8];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Bounded wait on an mbarrier phase.  Returns false when the shared abort
+// flag is raised or the cycle budget runs out (then it raises the flag and
+// records `site`).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           const FwdParams& p, int site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (static_cast<unsigned long long>(clock64() - t0) > p.wait_limit) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0, site);
+            return false;
+        }
+    }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void tile_range(const FwdParams& p, int qs, int& lo, int& hi) {
+    const int qe = min(qs + Cfg::BM, p.N) - 1;
+    lo = p.window > 0 ? max(0, qs - p.window + 1) / Cfg::BN : 0;
+    hi = p.causal ? qe / Cfg::BN : (p.N - 1) / Cfg::BN;
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+    constexpr int D = Cfg::D, BN = Cfg::BN, NQ = Cfg::NQ, BM = Cfg::BM, NSTAGE = Cfg::NSTAGE;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;                                       // NQ x Q tile
+    uint8_t* sKV = smem + NQ * Cfg::Q_TILE_BYTES;             // NSTAGE x KV tile
+    SharedBarriers* bars = reinterpret_cast<SharedBarriers*>(sKV + NSTAGE * Cfg::KV_TILE_BYTES);
+    volatile int* abort_flag = &bars->abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Work item: heaviest query blocks first when causal.
+    const int BH = p.B * p.H;
+    int mb, bh;
+    if (p.causal) {
+        mb = p.n_mblocks - 1 - static_cast<int>(blockIdx.x / BH);
+        bh = static_cast<int>(blockIdx.x % BH);
+    } else {
+        mb = static_cast<int>(blockIdx.x % p.n_mblocks);
+        bh = static_cast<int>(blockIdx.x / p.n_mblocks);
+    }
+    const int b = bh / p.H, h = bh % p.H;
+    const int q0 = mb * NQ * BM;
+
+    int lo[NQ], hi[NQ];
+    bool active[NQ];
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) {
+        active[t] = (q0 + t * BM) < p.N;
+        tile_range<Cfg>(p, q0 + t * BM, lo[t], hi[t]);
+    }
+    int u_lo = lo[0], u_hi = hi[0];
+#pragma unroll
+    for (int t = 1; t < NQ; ++t)
+        if (active[t]) {
+            u_lo = min(u_lo, lo[t]);
+            u_hi = max(u_hi, hi[t]);
+        }
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bars->q_full[t], 1);
+            mbar_init(&bars->s_full[t], 1);
+            mbar_init(&bars->p_full[t], 128);
+            mbar_init(&bars->o_full[t], 1);
+        }
+        mbar_init(&bars->drain, 1);
+        for (int s = 0; s < 8; ++s) {
+            mbar_init(&bars->ring_full[s], 1);
+            mbar_init(&bars->ring_empty[s], 1);
+        }
+        bars->abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == Cfg::LOAD_WARP && lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(&bars->tmem_base, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == Cfg::LOAD_WARP) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_q = l2_policy_evict_first();
+            const uint64_t pol_kv = l2_policy_evict_last();
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) {
+                if (!active[t]) continue;
+                mbar_arrive_expect_tx(&bars->q_full[t], Cfg::Q_TILE_BYTES);
+#pragma unroll
+                for (int cb = 0; cb < Cfg::NCB; ++cb)
+                    tma_load_4d(sQ + t * Cfg::Q_TILE_BYTES + cb * (BM * 128), &tmap_q, &bars->q_full[t],
+                                cb * Cfg::BOX_ELEMS, h, q0 + t * BM, b, pol_q);
+            }
+            uint32_t it = 0;
+            bool ok = true;
+            for (int j = u_lo; j <= u_hi && ok; ++j) {
+#pragma unroll
+                for (int kind = 0; kind < 2; ++kind) {
+                    const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
+                    if (!wait_phase(&bars->ring_empty[stage], (round & 1) ^ 1, abort_flag, p, SITE_LOAD_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars->ring_full[stage], Cfg::KV_TILE_BYTES);
+                    uint8_t* dst = sKV + stage * Cfg::KV_TILE_BYTES;
+                    const CUtensorMap* map = kind == 0 ? &tmap_k : &tmap_v;
+#pragma unroll
+                    for (int cb = 0; cb < Cfg::NCB; ++cb)
+                        tma_load_4d(dst + cb * (BN * 128), map, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS, h,
+                                    j * BN, b, pol_kv);
+                    ++it;
+                }
+            }
+            if (!ok) {
+                // Let copies already in flight land before the CTA exits.
+                const uint32_t first = it > NSTAGE ? it - NSTAGE : 0;
+                for (uint32_t k = first; k < it; ++k) {
+                    const uint32_t stage = k % NSTAGE, round = k / NSTAGE;
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(&bars->ring_full[stage], round & 1) &&
+                           static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == Cfg::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t fmt = Cfg::FP8 ? 0u : 1u;
+            constexpr uint32_t idesc_s = make_idesc(fmt, 128, BN, 0);
+            constexpr uint32_t idesc_o = make_idesc(fmt, 128, D, 1);
+            const uint32_t sQ_addr = smem_u32(sQ);
+            const uint32_t sKV_addr = smem_u32(sKV);
+            bool ok = true;
+#pragma unroll
+            for (int t = 0; t < NQ; ++t)
+                if (active[t] && ok) ok = wait_phase(&bars->q_full[t], 0, abort_flag, p, SITE_MMA_Q);
+            uint32_t it = 0;
+            uint32_t pv_count[NQ];
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) pv_count[t] = 0;
+            uint32_t prev_v_stage = 0, prev_v_round = 0;
+
+            auto issue_pv = [&](int t, int j, uint32_t vstage) {
+                const uint32_t v_base = sKV_addr + vstage * Cfg::KV_TILE_BYTES;
+                const uint32_t p_tmem = tmem + t * Cfg::S_COL;
+                const uint32_t o_tmem = tmem + Cfg::O_COL0 + t * D;
+#pragma unroll
+                for (int kk = 0; kk < BN / Cfg::MMA_K; ++kk) {
+                    const uint64_t bdesc = sdesc_sw128(v_base + kk * Cfg::MMA_K * 128, BN * 128, 1024);
+                    const uint32_t acc = (pv_count[t] > 0 || kk > 0) ? 1u : 0u;
+                    if constexpr (Cfg::FP8)
+                        mma_f8_ts(o_tmem, p_tmem + kk * (Cfg::MMA_K / 4), bdesc, idesc_o, acc);
+                    else
+                        mma_f16_ts(o_tmem, p_tmem + kk * (Cfg::MMA_K / 2), bdesc, idesc_o, acc);
+                }
+                ++pv_count[t];
+                if (j == hi[t]) mma_commit(&bars->o_full[t]);
+            };
+
+            for (int u = u_lo; u <= u_hi && ok; ++u) {
+                const uint32_t kstage = it % NSTAGE, kround = it / NSTAGE;
+                ++it;
+                const uint32_t vstage = it % NSTAGE, vround = it / NSTAGE;
+                ++it;
+                if (!wait_phase(&bars->ring_full[kstage], kround & 1, abort_flag, p, SITE_MMA_FULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                bool v_ready = false;
+#pragma unroll
+                for (int t = 0; t < NQ; ++t) {
+                    if (!active[t]) continue;
+                    if (u > u_lo && u - 1 >= lo[t] && u - 1 <= hi[t]) {
+                        if (!v_ready) {
+                            if (!wait_phase(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p,
+                                            SITE_MMA_FULL)) {
+                                ok = false;
+                                break;
+                            }
+                            v_ready = true;
+                        }
+                        if (!wait_phase(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(t, u - 1, prev_v_stage);
+                    }
+                    if (u >= lo[t] && u <= hi[t]) {
+                        const uint32_t q_base = sQ_addr + t * Cfg::Q_TILE_BYTES;
+                        const uint32_t k_base = sKV_addr + kstage * Cfg::KV_TILE_BYTES;
+                        const uint32_t s_tmem = tmem + t * Cfg::S_COL;
+#pragma unroll
+                        for (int kk = 0; kk < D / Cfg::MMA_K; ++kk) {
+                            const int byte_k = kk * Cfg::MMA_K * Cfg::ES;
+                            const uint32_t a_off = (byte_k / 128) * (BM * 128) + (byte_k % 128);
+                            const uint32_t b_off = (byte_k / 128) * (BN * 128) + (byte_k % 128);
+                            const uint64_t adesc = sdesc_sw128(q_base + a_off, 16, 1024);
+                            const uint64_t bdesc = sdesc_sw128(k_base + b_off, 16, 1024);
+                            if constexpr (Cfg::FP8)
+                                mma_f8_ss(s_tmem, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                            else
+                                mma_f16_ss(s_tmem, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars->s_full[t]);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&bars->ring_empty[kstage]);
+                if (u > u_lo) mma_commit(&bars->ring_empty[prev_v_stage]);
+                prev_v_stage = vstage;
+                prev_v_round = vround;
+            }
+            if (ok) {
+                // P V of the last key tile.
+                ok = wait_phase(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p, SITE_MMA_FULL);
+#pragma unroll
+                for (int t = 0; t < NQ && ok; ++t) {
+                    if (!active[t] || u_hi < lo[t] || u_hi > hi[t]) continue;
+                    if (!wait_phase(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(t, u_hi, prev_v_stage);
+                }
+                if (ok) mma_commit(&bars->ring_empty[prev_v_stage]);
+            }
+            // Every MMA this thread issued has finished before teardown.
+            mma_commit(&bars->drain);
+            wait_phase(&bars->drain, 0, abort_flag, p, SITE_MMA_DRAIN);
+        }
+        __syncwarp();
+    } else if (warp < 4 * NQ) {
+        // ------------------------------------------------------------ softmax
+        const int t = warp >> 2;
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;
+        const int qs = q0 + t * BM;
+        const int i = qs + r;                                  // query row
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_off + t * Cfg::S_COL;
+        const uint32_t o_tmem = tmem + lane_off + Cfg::O_COL0 + t * D;
+        // Visible keys of row i: [klo, khi].
+        const int klo = p.window > 0 ? i - p.window + 1 : 0;
+        const int khi = p.causal ? min(i, p.N - 1) : p.N - 1;
+        const int nblk = (p.N + 127) / 128;
+
+        float vmax = 1.0f;
+        float q_mult = p.scale_log2;
+        if constexpr (Cfg::FP8) {
+            const float* vs = p.v_scale + static_cast<size_t>(bh) * nblk;
+            vmax = 0.0f;
+            for (int x = 0; x < nblk; ++x) vmax = fmaxf(vmax, vs[x]);
+            if (!(vmax > 0.0f)) vmax = 1.0f;
+            q_mult *= p.q_scale[static_cast<size_t>(bh) * nblk + qs / 128];
+        }
+
+        float m = -INFINITY;   // running max of the log2-scaled scores
+        float l = 0.0f;        // running sum of exp2(score - m)
+        uint32_t count = 0;
+        bool ok = active[t];
+        if (ok) {
+            for (int j = lo[t]; j <= hi[t]; ++j) {
+                bool w = wait_phase(&bars->s_full[t], count & 1, abort_flag, p, SITE_SOFTMAX_S);
+                if (!__all_sync(0xffffffffu, w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float mult = q_mult;
+                float pv_mult = 1.0f;
+                if constexpr (Cfg::FP8) {
+                    const size_t sb = static_cast<size_t>(bh) * nblk + (j * BN) / 128;
+                    mult *= p.k_scale[sb];
+                    pv_mult = 256.0f * (p.v_scale[sb] / vmax);
+                }
+                uint32_t sr[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tmem + c * 32, sr + c * 32);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) reg_fence32(sr + c * 32);
+                float* s = reinterpret_cast<float*>(sr);
+
+                const int kbase = j * BN;
+                if (kbase < klo || kbase + BN - 1 > khi) {
+#pragma unroll
+                    for (int c = 0; c < BN; ++c) {
+                        const int key = kbase + c;
+                        if (key < klo || key > khi) s[c] = -INFINITY;
+                    }
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+                const float m_new = fmaxf(m, mx * mult);
+                const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+                const float alpha = ex2_approx(m - m_use);
+                const float neg = -m_use;
+                float rsum = 0.0f;
+                if constexpr (!Cfg::FP8) {
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * x], mult, neg));
+                            const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * x + 1], mult, neg));
+                            rsum += p0 + p1;
+                            pk[x] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(s_tmem + c * 16, pk);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN / 64; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) {
+                            float e[4];
+#pragma unroll
+                            for (int y = 0; y < 4; ++y) {
+                                e[y] = ex2_approx(fmaf(s[c * 64 + 4 * x + y], mult, neg));
+                                rsum += e[y];
+                            }
+                            pk[x] = pack_e4m3x4(e[0] * pv_mult, e[1] * pv_mult, e[2] * pv_mult, e[3] * pv_mult);
+                        }
+                        tmem_st16(s_tmem + c * 16, pk);
+                    }
+                }
+                l = l * alpha + rsum;
+                // Rescale the accumulator of the rows whose maximum moved.  The
+                // commit that signalled S_t(j) also covers O_t += P_t V_{j-1}, so
+                // O_t is stable here; the next P V waits for p_full below.
+                if (count > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t orr[32];
+                        tmem_ld32(o_tmem + c * 32, orr);
+                        tmem_wait_ld();
+                        reg_fence32(orr);
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * alpha);
+                        tmem_st32(o_tmem + c * 32, orr);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars->p_full[t]);
+                m = m_use;
+                ++count;
+            }
+        }
+        if (ok) {
+            bool w = wait_phase(&bars->o_full[t], 0, abort_flag, p, SITE_SOFTMAX_O);
+            ok = __all_sync(0xffffffffu, w);
+        }
+        if (ok) {
+            tc_fence_after();
+            float out_mult = 1.0f / l;
+            if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / 256.0f);
+            const bool store = i < p.N;
+            __nv_bfloat16* orow =
+                reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * p.N + i) * p.H + h) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(o_tmem + c * 32, orr);
+                tmem_wait_ld();
+                reg_fence32(orr);
+                uint32_t pk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x)
+                    pk[x] = pack_bf16x2(__uint_as_float(orr[2 * x]) * out_mult,
+                                        __uint_as_float(orr[2 * x + 1]) * out_mult);
+                if (store) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+                }
+            }
+            if (store) p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.69314718055994530942f;
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace attn

@@ -1,0 +1,47 @@
+// Host-side launch of one instantiation of the fused forward kernel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+
+struct FwdMaps {
+    CUtensorMap q, k, v;
+};
+
+// Tile geometry an instantiation needs from the host (tensor-map boxes).
+struct FwdGeometry {
+    int d, bn, nq, elem_bytes, threads, smem_bytes, stages;
+};
+
+template <class Cfg>
+FwdGeometry fwd_geometry() {
+    return FwdGeometry{Cfg::D, Cfg::BN, Cfg::NQ, Cfg::ES, Cfg::THREADS, Cfg::SMEM_BYTES, Cfg::NSTAGE};
+}
+
+template <class Cfg>
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t stream) {
+    auto kernel = attn_fwd_kernel<Cfg>;
+    // The attribute is per function and per device; setting it is cheap and
+    // idempotent, so it is set on every launch (devices may differ per call).
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const long long units = static_cast<long long>(p.n_mblocks) * p.B * p.H;
+    kernel<<<dim3(static_cast<unsigned>(units)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream>>>(maps.q, maps.k,
+                                                                                               maps.v, p);
+    return cudaGetLastError();
+}
+
+// Per-instantiation entry points (one translation unit each).
+cudaError_t run_fwd_bf16_d64(const FwdMaps&, const FwdParams&, cudaStream_t);
+cudaError_t run_fwd_bf16_d128(const FwdMaps&, const FwdParams&, cudaStream_t);
+cudaError_t run_fwd_bf16_d256(const FwdMaps&, const FwdParams&, cudaStream_t);
+cudaError_t run_fwd_fp8_d128(const FwdMaps&, const FwdParams&, cudaStream_t);
+FwdGeometry geom_bf16_d64();
+FwdGeometry geom_bf16_d128();
+FwdGeometry geom_bf16_d256();
+FwdGeometry geom_fp8_d128();
+
+}  // namespace attn

@@ -1,0 +1,222 @@
+// FP8 prep kernel: r = x D H_d / sqrt(d) (Q and K, mode 1), then per block
+// of 128 tokens of one (batch, head): amax, scale = amax / 448, e4m3 codes
+// of r / scale.  FlashAttention-3 deep-reading report §2.2 and §3.3 (block
+// quantization; incoherent processing with M = diag(+-1) x Hadamard, O(d log d)).
+//
+// One CTA owns one 128-token block of one head, so the block amax is a CTA
+// reduction and the data is read once and written once (the op is bound by
+// device-memory bandwidth).  A warp holds whole rows: lane l keeps elements
+// [l*E, l*E + E) of a row, E = d / 32.  The Walsh-Hadamard butterflies with
+// stride < E stay inside a thread; the wider ones pair lanes with shuffles.
+// Mode 2 (one scale per tensor) runs three launches: block amax into
+// `scales`, a one-CTA reduction that turns them into the tensor's scale,
+// and the quantisation with that scale.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "fp8_prep.cuh"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBlockRows = 128;
+
+// Sign c of the +-1 diagonal: bit 63 of splitmix64 output c for state
+// `seed` (output c is the mixing function applied to seed + (c + 1) * gamma).
+__device__ __forceinline__ float diag_sign(unsigned long long seed, int c) {
+    unsigned long long z = seed + static_cast<unsigned long long>(c + 1) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return (z >> 63) ? -1.0f : 1.0f;
+}
+
+enum Pass { kFused = 0, kAmaxOnly = 1, kApplyScale = 2 };
+
+template <int D, int WARPS, int PASS>
+__global__ void __launch_bounds__(WARPS * 32)
+    fp8_prep_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ x8, float* __restrict__ scales,
+                    int H, int N, int nblk, int rotate, unsigned long long seed) {
+    constexpr int E = D / 32;                     // elements per lane
+    constexpr int RPW = kBlockRows / WARPS;       // rows per warp
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int blk = blockIdx.x % nblk;
+    const int bh = blockIdx.x / nblk;
+    const int b = bh / H, h = bh % H;
+    const int n0 = blk * kBlockRows;
+
+    float r[RPW][E];
+    float sgn[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) sgn[e] = rotate ? diag_sign(seed, lane * E + e) : 1.0f;
+
+    float amax = 0.0f;
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int n = n0 + warp * RPW + rr;
+        if (n < N) {
+            const __nv_bfloat16* src = x + ((static_cast<size_t>(b) * N + n) * H + h) * D + lane * E;
+            if constexpr (E == 2) {
+                const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(src);
+                r[rr][0] = __bfloat162float(v.x);
+                r[rr][1] = __bfloat162float(v.y);
+            } else if constexpr (E == 4) {
+                const uint2 v = *reinterpret_cast<const uint2*>(src);
+                const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    r[rr][2 * k] = __bfloat162float(pv[k].x);
+                    r[rr][2 * k + 1] = __bfloat162float(pv[k].y);
+                }
+            } else {
+                const uint4 v = *reinterpret_cast<const uint4*>(src);
+                const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    r[rr][2 * k] = __bfloat162float(pv[k].x);
+                    r[rr][2 * k + 1] = __bfloat162float(pv[k].y);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) r[rr][e] = 0.0f;
+        }
+        if (rotate) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) r[rr][e] *= sgn[e];
+            // Butterflies inside the thread (strides 1 .. E/2).
+#pragma unroll
+            for (int s = 1; s < E; s <<= 1) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if ((e & s) == 0) {
+                        const float a = r[rr][e], c = r[rr][e + s];
+                        r[rr][e] = a + c;
+                        r[rr][e + s] = a - c;
+                    }
+                }
+            }
+            // Butterflies across lanes (strides E .. D/2).
+#pragma unroll
+            for (int ls = 1; ls < 32; ls <<= 1) {
+                const bool upper = (lane & ls) != 0;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float other = __shfl_xor_sync(0xffffffffu, r[rr][e], ls);
+                    r[rr][e] = upper ? (other - r[rr][e]) : (r[rr][e] + other);
+                }
+            }
+            constexpr float inv_sqrt_d = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) r[rr][e] *= inv_sqrt_d;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(r[rr][e]));
+    }
+
+    __shared__ float warp_max[WARPS];
+    __shared__ float block_scale;
+    if constexpr (PASS != kApplyScale) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) warp_max[warp] = amax;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float a = warp_max[0];
+#pragma unroll
+            for (int w = 1; w < WARPS; ++w) a = fmaxf(a, warp_max[w]);
+            if constexpr (PASS == kAmaxOnly) {
+                scales[static_cast<size_t>(bh) * nblk + blk] = a;
+            } else {
+                const float s = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
+                scales[static_cast<size_t>(bh) * nblk + blk] = s;
+                block_scale = s;
+            }
+        }
+        if constexpr (PASS == kAmaxOnly) return;
+        __syncthreads();
+    } else {
+        if (threadIdx.x == 0) block_scale = scales[static_cast<size_t>(bh) * nblk + blk];
+        __syncthreads();
+    }
+    const float s = block_scale;
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int n = n0 + warp * RPW + rr;
+        if (n >= N) continue;
+        uint8_t* dst = x8 + ((static_cast<size_t>(b) * N + n) * H + h) * D + lane * E;
+        if constexpr (E == 2) {
+            uint16_t v;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                : "=h"(v)
+                : "f"(__fdiv_rn(r[rr][1], s)), "f"(__fdiv_rn(r[rr][0], s)));
+            *reinterpret_cast<uint16_t*>(dst) = v;
+        } else if constexpr (E == 4) {
+            *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(__fdiv_rn(r[rr][0], s), __fdiv_rn(r[rr][1], s),
+                                                            __fdiv_rn(r[rr][2], s), __fdiv_rn(r[rr][3], s));
+        } else {
+            uint2 v;
+            v.x = pack_e4m3x4(__fdiv_rn(r[rr][0], s), __fdiv_rn(r[rr][1], s), __fdiv_rn(r[rr][2], s),
+                              __fdiv_rn(r[rr][3], s));
+            v.y = pack_e4m3x4(__fdiv_rn(r[rr][4], s), __fdiv_rn(r[rr][5], s), __fdiv_rn(r[rr][6], s),
+                              __fdiv_rn(r[rr][7], s));
+            *reinterpret_cast<uint2*>(dst) = v;
+        }
+    }
+}
+
+// Mode 2: the block maxima in `scales` -> one scale, written to every entry.
+__global__ void __launch_bounds__(1024) per_tensor_scale_kernel(float* scales, long long count) {
+    float a = 0.0f;
+    for (long long i = threadIdx.x; i < count; i += blockDim.x) a = fmaxf(a, scales[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+    __shared__ float wm[32];
+    __shared__ float result;
+    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = a;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.0f;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, wm[w]);
+        result = m > 0.0f ? __fdiv_rn(m, 448.0f) : 1.0f;
+    }
+    __syncthreads();
+    const float s = result;
+    for (long long i = threadIdx.x; i < count; i += blockDim.x) scales[i] = s;
+}
+
+template <int D, int WARPS>
+cudaError_t launch_prep(const void* x, void* x8, float* scales, int B, int H, int N, int mode,
+                        unsigned long long seed, bool is_v, cudaStream_t stream) {
+    const int nblk = (N + kBlockRows - 1) / kBlockRows;
+    const long long ctas = static_cast<long long>(B) * H * nblk;
+    if (ctas >= (1ll << 31)) return cudaErrorInvalidValue;
+    const auto* xb = static_cast<const __nv_bfloat16*>(x);
+    auto* q8 = static_cast<uint8_t*>(x8);
+    const int rotate = (mode == 1 && !is_v) ? 1 : 0;
+    const dim3 grid(static_cast<unsigned>(ctas)), block(WARPS * 32);
+    if (mode != 2) {
+        fp8_prep_kernel<D, WARPS, kFused><<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, rotate, seed);
+        return cudaGetLastError();
+    }
+    fp8_prep_kernel<D, WARPS, kAmaxOnly><<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, 0, seed);
+    per_tensor_scale_kernel<<<1, 1024, 0, stream>>>(scales, ctas);
+    fp8_prep_kernel<D, WARPS, kApplyScale><<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, 0, seed);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t run_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, int d, int mode,
+                         unsigned long long sign_seed, bool is_v, cudaStream_t stream) {
+    switch (d) {
+        case 64: return launch_prep<64, 8>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
+        case 128: return launch_prep<128, 8>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
+        case 256: return launch_prep<256, 16>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace attn

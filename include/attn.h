@@ -1,0 +1,138 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused exact-attention forward.
+ *
+ * What is computed (FlashAttention-3 deep-reading report, "第三层" intro and
+ * §3.1-§3.3; "Efficient Attention & FlashAttention", "数学机理"):
+ *
+ *     O   = softmax(scale * Q K^T + mask) V          per (batch, head)
+ *     LSE = log(sum_j exp(scale * q_i . k_j))        natural log, per row,
+ *                                                    over the visible keys
+ *
+ * evaluated tile by tile with an online softmax (running row max m, running
+ * row sum l, the O accumulator rescaled when m grows, one division by l at
+ * the end) so that the N x N score matrix never reaches device memory.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout (the practitioner's FA3 re-test post, §4.2): Q, K, V and O are
+ *    contiguous (batch B, seqlen N, heads H, head_dim d) tensors, d fastest;
+ *    LSE is a contiguous (B, H, N) float32 tensor.
+ *  - d must be 64, 128 or 256.  B, H, N >= 0; an empty problem is a no-op.
+ *  - Mask: key j is visible to query i iff (causal == 0 || j <= i) and
+ *    (window <= 0 || j > i - window).  With causal != 0 and window = W > 0
+ *    each query sees the W most recent keys including itself (a sliding
+ *    window).  Key tiles that no query of a query tile can see are skipped,
+ *    not masked.
+ *  - scale <= 0 or non-finite selects 1 / sqrt(d).
+ *  - All pointers are DEVICE pointers, 16-byte aligned, owned by the
+ *    caller; the library allocates no device memory per call and keeps no
+ *    reference after the call returns.  Tensor memory (TMEM) is allocated and
+ *    freed inside each kernel.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Argument errors are detected before any launch.
+ *  - Return value: ATTN_OK or a negative attn_status.  The text of the last
+ *    error of the calling thread is available from attn_last_error_string().
+ *  - Rows that can see no key (only possible with a window and no causal
+ *    mask at the sequence end) get O = 0 and LSE = -inf.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1,    /* bad pointer, size, alignment or mode      */
+    ATTN_ERR_UNSUPPORTED = -2,    /* head_dim / device not supported           */
+    ATTN_ERR_CUDA = -3,           /* a CUDA runtime / driver call failed       */
+    ATTN_ERR_DEVICE_TIMEOUT = -4  /* a kernel gave up waiting (see below)      */
+} attn_status;
+
+/*
+ * attn_fwd -- bf16 fused attention forward.
+ *   q, k, v : const bf16 (B, N, H, d)
+ *   o       : bf16 (B, N, H, d), written
+ *   lse     : float32 (B, H, N), written
+ * The exponentials, the running max/sum and the accumulators are float32;
+ * P is rounded to bf16 for the P V product; the row sum l is accumulated
+ * from the unrounded float32 probabilities.
+ * Design (deep-reading report §3.1, §3.2): TMA-fed K/V shared-memory ring,
+ * warp-specialised load / MMA / softmax roles, tcgen05 MMAs with the S and
+ * O accumulators in tensor memory.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int N, int d, int causal, float scale, int window,
+             void* stream);
+
+/*
+ * attn_fwd_fp8 -- FP8 (e4m3) fused attention forward (deep-reading report
+ * §2.2 and §3.3: block quantization and incoherent processing).
+ *   q8, k8, v8          : const e4m3 (B, N, H, d) from attn_fp8_prep
+ *   q_scale, k_scale,
+ *   v_scale             : const float32 (B, H, ceil(N / 128)): the scale of
+ *                         each 128-token block, so that the real value of an
+ *                         element is scale * e4m3 value
+ *   o                   : bf16 (B, N, H, d), written
+ *   lse                 : float32 (B, H, N), written
+ * Q and K must have been rotated with the same seed (or not at all); the
+ * rotation leaves Q K^T unchanged.  V's block scale lies on the contraction
+ * dimension of P V, so it is folded into P before P is rounded to e4m3:
+ * P8 = e4m3(P * 256 * v_scale_j / vmax) with vmax the largest V block scale
+ * of the (batch, head); O = (sum P8 V8) * vmax / (256 * l).  Only d = 128 is
+ * supported (ATTN_ERR_UNSUPPORTED otherwise).
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+                 int B, int H, int N, int d, int causal, float scale, int window,
+                 const float* q_scale, const float* k_scale, const float* v_scale,
+                 void* stream);
+
+/*
+ * attn_fp8_prep -- fused rotation + block quantisation of one tensor
+ * (deep-reading report §2.2 / §3.3).
+ *   x      : const bf16 (B, N, H, d)
+ *   x8     : e4m3 (B, N, H, d), written
+ *   scales : float32 (B, H, ceil(N / block_rows)), written
+ *   block_rows : tokens per scale block; must be 128
+ *   mode   : 0 = per-block scales;
+ *            1 = per-block scales after incoherent processing
+ *                r = x D H_d / sqrt(d)  (D = diag(+-1) from sign_seed,
+ *                H_d the Sylvester Hadamard matrix); skipped when is_v != 0;
+ *            2 = one scale for the whole tensor (the per-tensor baseline),
+ *                stored in every entry of `scales`.
+ *   sign_seed : seed of the +-1 diagonal: sign c is -1 iff bit 63 of
+ *            splitmix64 output c (state = sign_seed) is set.
+ *   is_v   : nonzero for V (never rotated).
+ * scale = amax / 448 of the block (1 for an all-zero block); each element is
+ * r / scale rounded to nearest-even e4m3 and saturated to +-448.  amax, the
+ * scale and the division are float32.
+ */
+int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, int d,
+                  int block_rows, int mode, unsigned long long sign_seed, int is_v,
+                  void* stream);
+
+/*
+ * attn_device_status -- waits for `stream`, then reads and clears the
+ * library's device status word.  Every wait inside the kernels is bounded;
+ * a kernel that gives up records the site in this word and returns instead
+ * of hanging.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT (*site, if not NULL,
+ * receives the site code) or ATTN_ERR_CUDA.
+ */
+int attn_device_status(void* stream, int* site);
+
+/*
+ * attn_set_wait_limit -- cycles (SM clock) a kernel waits on one barrier
+ * before giving up; 0 restores the default (about two seconds).  Applies to
+ * launches made after the call, from any thread.
+ */
+int attn_set_wait_limit(unsigned long long cycles);
+
+/* Text of the last error of the calling thread ("" if none). */
+const char* attn_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

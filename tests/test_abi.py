@@ -1,0 +1,78 @@
+"""The C ABI library: it builds, loads without a GPU, exports every entry
+point include/attn.h declares, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_71_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.library()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_fwd_fp8", "attn_fp8_prep", "attn_last_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # never dereferenced: the checks fail first
+
+
+@pytest.mark.parametrize("d", [32, 96, 512])
+def test_unsupported_head_dim_rejected(lib, d):
+    rc = lib.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, d, 0, 0.0, 0, None)
+    assert rc == -2
+    assert b"head_dim" in lib.attn_last_error_string()
+
+
+def test_negative_sizes_and_window_rejected(lib):
+    assert lib.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 1, 16, 128, 0, 0.0, 0, None) == -1
+    assert lib.attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 128, 0, 0.0, -5, None) == -1
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    assert lib.attn_fwd(None, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 128, 0, 0.0, 0, None) == -1
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.attn_fwd(FAKE, odd, FAKE, FAKE, FAKE, 1, 1, 16, 128, 0, 0.0, 0, None) == -1
+    assert b"aligned" in lib.attn_last_error_string()
+
+
+def test_empty_problem_is_ok_without_launch(lib):
+    assert lib.attn_fwd(None, None, None, None, None, 0, 4, 16, 128, 1, 0.0, 0, None) == 0
+    assert lib.attn_fwd(None, None, None, None, None, 2, 4, 0, 128, 1, 0.0, 0, None) == 0
+
+
+def test_fp8_arguments_checked(lib):
+    assert lib.attn_fwd_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, 0, 0.0, 0, FAKE, FAKE, FAKE, None) == -2
+    assert lib.attn_fwd_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 128, 0, 0.0, 0, None, FAKE, FAKE, None) == -1
+
+
+def test_prep_arguments_checked(lib):
+    assert lib.attn_fp8_prep(FAKE, FAKE, FAKE, 1, 1, 16, 128, 64, 1, 0, 0, None) == -2
+    assert lib.attn_fp8_prep(FAKE, FAKE, FAKE, 1, 1, 16, 128, 128, 3, 0, 0, None) == -1
+    assert lib.attn_fp8_prep(FAKE, FAKE, FAKE, 1, 1, 16, 96, 128, 1, 0, 0, None) == -2
+    assert lib.attn_fp8_prep(None, None, None, 1, 1, 0, 128, 128, 1, 0, 0, None) == 0
+
+
+def test_wait_limit_setter(lib):
+    assert lib.attn_set_wait_limit(0) == 0

@@ -1,0 +1,115 @@
+"""bf16 fused forward vs the fp64 oracle on the same seeded inputs, through
+the C ABI (max-abs <= 1e-2, RMS <= 2e-3, LSE <= 1e-3)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_71_gb300 import api, synth
+from tests.helpers import assert_bf16_parity, errors, gpu_rows, lse_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(B, N, H, d, causal=False, window=0, seed=0, rows=None, scale=None):
+    q, k, v = synth.qkv_bf16(B, N, H, d, seed=seed)
+    o, lse = api.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=causal, window=window, scale=scale)
+    torch.cuda.synchronize()
+    if rows is None:
+        rows = np.arange(N, dtype=np.int32)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, window=window, rows=rows, scale=scale)
+    e = errors(gpu_rows(o, rows), o_ref, lse_rows(lse, rows), lse_ref)
+    rc, site = api.device_status()
+    assert rc == 0, f"device status {rc} site {site:#x}"
+    return e
+
+
+def test_config1_small_noncausal():
+    """B=1, H=2, N=256, d=64, non-causal, scale 1/sqrt(d), seed 0."""
+    e = run_case(1, 256, 2, 64, causal=False)
+    assert_bf16_parity(e, "C1")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_multi_tile(d, causal):
+    e = run_case(1, 1000, 2, d, causal=causal, seed=1)
+    assert_bf16_parity(e, f"N=1000 d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("N", [1, 5, 77, 128, 129, 255, 256, 257, 383])
+def test_short_and_boundary_lengths(N):
+    for causal in (False, True):
+        e = run_case(2, N, 3, 128, causal=causal, seed=N)
+        assert_bf16_parity(e, f"N={N} causal={causal}")
+
+
+@pytest.mark.parametrize("window", [1, 127, 128, 129, 300, 5000])
+def test_sliding_window(window):
+    e = run_case(1, 1500, 2, 128, causal=True, window=window, seed=3)
+    assert_bf16_parity(e, f"window={window}")
+
+
+def test_window_without_causal():
+    e = run_case(1, 700, 2, 64, causal=False, window=200, seed=4)
+    assert_bf16_parity(e, "non-causal window")
+
+
+def test_explicit_scale():
+    e = run_case(1, 300, 2, 128, causal=True, seed=5, scale=0.05)
+    assert_bf16_parity(e, "scale=0.05")
+
+
+def test_config2_full_size_sampled_rows():
+    """B=2, H=32, N=4096, d=128, causal (the benchmark workload)."""
+    rows = synth.sample_rows(4096, 96, seed=0, must=(4095, 2047, 2048))
+    e = run_case(2, 4096, 32, 128, causal=True, rows=rows)
+    assert_bf16_parity(e, "C2")
+
+
+def test_config5_long_window_sampled_rows():
+    """B=1, H=8, N=32768, d=128, causal, 4096-token window."""
+    rows = synth.sample_rows(32768, 512, seed=5, must=(0, 127, 128, 4095, 4096, 4097, 32767))
+    e = run_case(1, 32768, 8, 128, causal=True, window=4096, rows=rows)
+    assert_bf16_parity(e, "C5")
+
+
+def test_empty_problem_is_a_noop():
+    x = torch.empty((1, 0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    o, lse = api.attn_fwd(x, x, x)
+    assert o.numel() == 0 and lse.numel() == 0
+
+
+def test_outputs_written_exactly_once_and_nothing_outside():
+    """NaN-prefilled outputs inside larger guard buffers: every element of O
+    and LSE is written, nothing past them is touched."""
+    B, N, H, d = 1, 300, 2, 128
+    q, k, v = synth.qkv_bf16(B, N, H, d, seed=6)
+    guard = 4096
+    ob = torch.full((B * N * H * d + guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lb = torch.full((B * H * N + guard,), float("nan"), dtype=torch.float32, device="cuda")
+    o = ob[: B * N * H * d].view(B, N, H, d)
+    lse = lb[: B * H * N].view(B, H, N)
+    api.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+    assert torch.isnan(ob[B * N * H * d:]).all() and torch.isnan(lb[B * H * N:]).all()
+
+
+def test_repeat_is_bitwise_deterministic():
+    q, k, v = (to_dev(t) for t in synth.qkv_bf16(1, 900, 4, 128, seed=7))
+    o1, l1 = api.attn_fwd(q, k, v, causal=True)
+    o2, l2 = api.attn_fwd(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("N", [512, 2048, 16384])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_config3_sweep_sampled_rows(N, d, causal):
+    """16384 tokens, hidden 2048: B = 16384 / N, H = 2048 / d."""
+    B, H = 16384 // N, 2048 // d
+    rows = synth.sample_rows(N, 24, seed=N + d)
+    e = run_case(B, N, H, d, causal=causal, rows=rows, seed=11)
+    assert_bf16_parity(e, f"C3 N={N} d={d} causal={causal}")
