@@ -1,0 +1,451 @@
+"""Benchmark of the fused exact-attention forward on GB300.
+
+Default workload: bf16 forward, B=2, H=32, N=4096, d=128, causal (the
+headline configuration), FLOPs counted as 4 B H N^2 d / 2.  One step = one
+fused forward over the batch (load, QK^T, online softmax, correction, PV and
+epilogue all inside one kernel launch).  The FP8 path (prep of Q, K, V with
+block scales + Hadamard rotation, then the FP8 forward) is measured on its
+own workload (B=2, H=16, N=8192, d=128, non-causal, outlier inputs) and
+reported in the "fp8" object of the same line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload c2|c4|c5|c3:N:d:causal] [--quick]
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
+device (weak scaling, no collective on the data path); `value` is the work of
+all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (bf16, fp8) on 1 GB300 and % of dense tensor peak"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+WORKLOADS = {
+    "c2": dict(name="bf16 fwd B=2 H=32 N=4096 d=128 causal", B=2, H=32, N=4096, d=128, causal=True, window=0,
+               dtype="bf16"),
+    "c4": dict(name="fp8 e4m3 fwd B=2 H=16 N=8192 d=128 non-causal, outliers, block scales + Hadamard",
+               B=2, H=16, N=8192, d=128, causal=False, window=0, dtype="fp8"),
+    "c5": dict(name="bf16 fwd B=1 H=8 N=32768 d=128 causal, 4096-token sliding window", B=1, H=8, N=32768,
+               d=128, causal=True, window=4096, dtype="bf16"),
+}
+
+
+def workload(spec: str) -> dict:
+    if spec in WORKLOADS:
+        return dict(WORKLOADS[spec])
+    if spec.startswith("c3:"):
+        _, n, d, c = spec.split(":")
+        n, d, c = int(n), int(d), c in ("1", "true", "causal")
+        return dict(name=f"bf16 fwd sweep point N={n} d={d} {'causal' if c else 'non-causal'} (16384 tokens, "
+                         f"hidden 2048)", B=16384 // n, H=2048 // d, N=n, d=d, causal=c, window=0, dtype="bf16")
+    raise SystemExit(f"unknown workload {spec}")
+
+
+def attended_pairs(N: int, causal: bool, window: int) -> int:
+    """Exact count of visible (query, key) pairs of one head."""
+    i = np.arange(N, dtype=np.int64)
+    hi = i if causal else np.full(N, N - 1)
+    lo = np.maximum(0, i - window + 1) if window > 0 else np.zeros(N, dtype=np.int64)
+    return int(np.sum(hi - lo + 1))
+
+
+def flops_per_step(w: dict) -> float:
+    """4 B H N^2 d, halved when causal; with a window, the attended pairs."""
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    if w["window"] > 0:
+        return 4.0 * B * H * d * attended_pairs(N, w["causal"], w["window"])
+    return 4.0 * B * H * N * N * d / (2.0 if w["causal"] else 1.0)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_71_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(f"{kernel}/{workload_key}")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            rows.append(parts)
+        if not rows and self.lines:   # uuid formats differ: take the first GPU listed
+            first = self.lines[0].split(",")[0].strip()
+            rows = [[p.strip() for p in ln.split(",")] for ln in self.lines if ln.split(",")[0].strip() == first]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_inputs(w, device, seed=0):
+    """Seeded synthetic inputs on the device (bf16 bit patterns from synth)."""
+    import torch
+
+    from exact_attention_71_gb300 import synth
+    outliers = w["dtype"] == "fp8"
+    arrs = synth.qkv_bf16(w["B"], w["N"], w["H"], w["d"], seed=seed, outliers=outliers)
+    return [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device) for a in arrs], arrs
+
+
+def time_loop(fn, steps, stream):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def cpu_baseline(w, budget_s=12.0, arrs=None):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample of
+    query rows of the same workload; throughput in the same unit (TFLOPS of
+    attention arithmetic, 4 d per attended pair)."""
+    import oracle
+
+    from exact_attention_71_gb300 import synth
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    if arrs is None:
+        arrs = synth.qkv_bf16(B, N, H, d, seed=0, outliers=w["dtype"] == "fp8")
+    q, k, v = arrs
+    cores = os.cpu_count() or 1
+
+    def pairs_of(rows):
+        rows = np.asarray(rows, dtype=np.int64)
+        hi = rows if w["causal"] else np.full(len(rows), N - 1)
+        lo = np.maximum(0, rows - w["window"] + 1) if w["window"] > 0 else np.zeros(len(rows), dtype=np.int64)
+        return int(np.sum(hi - lo + 1)) * B * H
+
+    nrows = 2
+    t = 0.0
+    while True:
+        rows = synth.sample_rows(N, nrows, seed=17)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, causal=w["causal"], window=w["window"], rows=rows, nthreads=cores)
+        t = time.perf_counter() - t0
+        if t >= budget_s / 4 or nrows >= N:
+            break
+        nrows = min(N, int(nrows * max(2.0, min(8.0, (budget_s / 4) / max(t, 1e-3)))))
+    flops = 4.0 * d * pairs_of(rows)
+    return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} seeded query rows per head x all {B * H} heads of the workload "
+                      f"({flops / 1e9:.2f} GFLOP in {t:.1f} s, fp64, {cores} threads)"}
+
+
+def run_reference(args, w, key):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    per = []
+    cb = None
+    for _ in range(args.warmup):
+        pass
+    for _ in range(max(1, args.steps)):
+        cb = cpu_baseline(w, budget_s=args.ref_budget)
+        per.append(cb["value"])
+    val = float(np.median(per))
+    cb["value"] = val
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "N": w["N"],
+                                             "d": w["d"], "causal": w["causal"], "window": w["window"]},
+            "cpu_baseline": cb, "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0},
+            "vs_baseline": None}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--quick", action="store_true", help="skip e2e, FP8 and CPU baseline (profiling runs)")
+    ap.add_argument("--ref-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    w = workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w, args.workload)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_71_gb300 import api
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    # Two resident input sets (> L2 each) used alternately, so no step finds
+    # the previous step's inputs in the 129 MB L2.
+    sets = []
+    arrs0 = None
+    for s in range(2):
+        (q, k, v), arrs = make_inputs(w, device, seed=s)
+        if s == 0:
+            arrs0 = arrs
+        if w["dtype"] == "fp8":
+            q8, k8, v8, qs, ks, vs = api.fp8_prepare_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, sign_seed=1234)
+            sets.append((q8, k8, v8, qs, ks, vs))
+        else:
+            sets.append((q, k, v))
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    step_idx = [0]
+
+    def step():
+        s = sets[step_idx[0] & 1]
+        step_idx[0] += 1
+        if w["dtype"] == "fp8":
+            api.attn_fwd_fp8(*s, causal=w["causal"], window=w["window"], out=o, lse=lse, stream=stream)
+        else:
+            api.attn_fwd(*s, causal=w["causal"], window=w["window"], out=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid if rank == 0 else None) as clk:
+        barrier()
+        ms = time_loop(step, args.steps, stream)
+        barrier()
+    t_local = torch.tensor([ms], dtype=torch.float64, device=device)
+    if ws > 1:
+        dist.all_reduce(t_local, op=dist.ReduceOp.MAX)
+    ms_total = float(t_local.item())
+    rc, site = api.device_status(stream)
+    if rc != 0:
+        raise SystemExit(f"device status {rc} (site {site:#x})")
+
+    flops = flops_per_step(w)
+    ms_step = ms_total / args.steps
+    value = ws * flops * args.steps / (ms_total / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    achieved = flops / (ms_step / 1e3) / 1e12
+    kernel = "attn_fwd_fp8" if w["dtype"] == "fp8" else "attn_fwd"
+    if w["dtype"] == "fp8":
+        fp8_peak = peaks.get("fp8_tflops") or 2.0 * peaks["bf16_tflops"]
+        peak, peak_note = fp8_peak, f"{peak_src} bf16 burst x 2 (nominal fp8:bf16 ratio)"
+    else:
+        peak, peak_note = peaks["bf16_tflops"], f"{peak_src} bf16 burst (cuBLAS)"
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel, args.workload),
+            "peak_source": peak_note,
+            "frac_of_sustained": round(achieved / (peaks.get("bf16_tflops_sustained", peak) *
+                                                   (2.0 if w["dtype"] == "fp8" else 1.0)), 4)}
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w["dtype"] == "bf16" else "e4m3", "data": "synthetic",
+            "config": {"workload": w["name"], "B": B, "H": H, "N": N, "d": d, "causal": w["causal"],
+                       "window": w["window"], "flops_per_step": flops,
+                       "flop_convention": "4 B H N^2 d, halved for causal; window: 4 d x attended pairs",
+                       "l2": "inputs larger than L2 (two resident input sets, alternated per step)",
+                       "parallelism": f"independent replicas x{ws}"},
+            "roofline": roof, "gpu_launches": args.steps, "clocks": clk.summary() if rank == 0 else None}
+
+    if not args.quick and rank == 0:
+        line["e2e"] = e2e_measure(api, w, device, stream, arrs0, flops, steps=min(args.steps, 20))
+        if w["dtype"] == "bf16" and args.workload == "c2":
+            line["fp8"] = fp8_secondary(api, device, stream, steps=min(args.steps, 200))
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.ref_budget, arrs=arrs0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def e2e_measure(api, w, device, stream, arrs, flops, steps):
+    """Same metric through the public API with HOST buffers: pinned host
+    Q, K, V copied to the device, the forward, O and LSE copied back, all
+    inside the timed region."""
+    import torch
+    hq, hk, hv = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in arrs)
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    dq, dk, dv = (torch.empty_like(t, device=device) for t in (hq, hk, hv))
+    do = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=device)
+    dl = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    ho = torch.empty((B, N, H, d), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    fp8 = w["dtype"] == "fp8"
+    launches = 4 if fp8 else 1
+
+    def step():
+        with torch.cuda.stream(stream):
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            if fp8:
+                q8, k8, v8, qs, ks, vs = api.fp8_prepare_qkv(dq, dk, dv, api.MODE_BLOCK_HADAMARD, 1234,
+                                                             stream=stream)
+                api.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=w["causal"], window=w["window"], out=do,
+                                 lse=dl, stream=stream)
+            else:
+                api.attn_fwd(dq, dk, dv, causal=w["causal"], window=w["window"], out=do, lse=dl, stream=stream)
+            ho.copy_(do, non_blocking=True)
+            hl.copy_(dl, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    ms = time_loop(step, steps, stream) / steps
+    h2d = 3 * hq.numel() * 2
+    d2h = ho.numel() * 2 + hl.numel() * 4
+    return {"value": round(flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "kernel_launches_per_step": launches}
+
+
+def fp8_secondary(api, device, stream, steps):
+    """FP8 path on its workload: prep (3 tensors) + FP8 forward, and the
+    forward alone."""
+    import torch
+    w = dict(WORKLOADS["c4"])
+    (q, k, v), _ = make_inputs(w, device, seed=0)
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    prepped = api.fp8_prepare_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, 1234, stream=stream)
+
+    def fwd_only():
+        api.attn_fwd_fp8(*prepped, causal=False, out=o, lse=lse, stream=stream)
+
+    def with_prep():
+        pp = api.fp8_prepare_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, 1234, stream=stream)
+        api.attn_fwd_fp8(*pp, causal=False, out=o, lse=lse, stream=stream)
+
+    flops = flops_per_step(w)
+    out = {"workload": w["name"], "flops_per_step": flops}
+    for name, fn in (("fwd", fwd_only), ("prep_plus_fwd", with_prep)):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(device)
+        ms = time_loop(fn, steps, stream) / steps
+        out[name] = {"ms": round(ms, 5), "tflops": round(flops / (ms / 1e3) / 1e12, 1)}
+    peaks, src = load_peaks()
+    fp8_peak = peaks.get("fp8_tflops") or 2.0 * peaks["bf16_tflops"]
+    out["frac_of_fp8_peak"] = round(out["fwd"]["tflops"] / fp8_peak, 4)
+    out["fp8_peak"] = fp8_peak
+    out["fp8_peak_source"] = f"{src} bf16 burst x 2 (nominal fp8:bf16 ratio)"
+    return out
+
+
+if __name__ == "__main__":
+    main()

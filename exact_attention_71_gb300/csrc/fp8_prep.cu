@@ -109,8 +109,10 @@ __global__ void __launch_bounds__(WARPS * 32)
                 }
             }
             constexpr float inv_sqrt_d = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
+            // "+ 0.0f" maps a -0 produced by a sign flip of an exact zero to +0,
+            // so a zero always encodes as the +0 code.
 #pragma unroll
-            for (int e = 0; e < E; ++e) r[rr][e] *= inv_sqrt_d;
+            for (int e = 0; e < E; ++e) r[rr][e] = __fadd_rn(r[rr][e] * inv_sqrt_d, 0.0f);
         }
 #pragma unroll
         for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(r[rr][e]));
