@@ -90,6 +90,17 @@ struct FwdCfg {
     static constexpr int MMA_WARP = NQ * 4 + 1;
     static constexpr int THREADS = NQ * 128 + 128;
     static constexpr int BAR_BYTES = 256;
+    // The reference maximum of a row moves only when the row maximum exceeds
+    // it by more than this (log2 units); 0 = exact tracking.
+    static constexpr float RESCALE_LOG2 = FP8 ? 0.0f : 8.0f;
+    // Register split: the launch gives every thread LAUNCH_REGS; the load /
+    // MMA warpgroup drops to LOW_REGS and the softmax warpgroups rise to
+    // HIGH_REGS.  The sum stays within the launch allocation.
+    static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 248 : (65536 / THREADS) / 8 * 8;
+    static constexpr int LOW_REGS = 72;
+    static constexpr int HIGH_REGS_RAW = ((LAUNCH_REGS * THREADS - LOW_REGS * 128) / (NQ * 128)) / 8 * 8;
+    static constexpr int HIGH_REGS = HIGH_REGS_RAW > 248 ? 248 : HIGH_REGS_RAW;
+    static_assert(HIGH_REGS * NQ * 128 + LOW_REGS * 128 <= LAUNCH_REGS * THREADS, "register split");
     static constexpr int SMEM_BYTES = 1024 + NQ * Q_TILE_BYTES + NSTAGE * KV_TILE_BYTES + BAR_BYTES;
 
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
@@ -211,6 +222,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
+    if (warp >= 4 * NQ) {
+    regs_decrease<Cfg::LOW_REGS>();
     if (warp == Cfg::LOAD_WARP) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -368,7 +381,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             wait_phase(&bars->drain, 0, abort_flag, p, SITE_MMA_DRAIN);
         }
         __syncwarp();
-    } else if (warp < 4 * NQ) {
+    }
+    } else {
+        regs_increase<Cfg::HIGH_REGS>();
         // ------------------------------------------------------------ softmax
         const int t = warp >> 2;
         const int quad = warp & 3;
@@ -418,34 +433,54 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) reg_fence32(sr + c * 32);
-                float* s = reinterpret_cast<float*>(sr);
 
                 const int kbase = j * BN;
                 if (kbase < klo || kbase + BN - 1 > khi) {
 #pragma unroll
                     for (int c = 0; c < BN; ++c) {
                         const int key = kbase + c;
-                        if (key < klo || key > khi) s[c] = -INFINITY;
+                        if (key < klo || key > khi) sr[c] = __float_as_uint(-INFINITY);
                     }
                 }
-                float mx = s[0];
+                // Row maximum: four independent chains of 3-input max.
+                float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+                float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
 #pragma unroll
-                for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
-                const float m_new = fmaxf(m, mx * mult);
-                const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+                for (int c = 4; c + 8 <= BN; c += 8) {
+                    mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
+                    mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                    mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                    mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+                }
+                mx0 = fmax3(mx0, mx1, __uint_as_float(sr[BN - 4]));
+                mx2 = fmax3(mx2, mx3, __uint_as_float(sr[BN - 3]));
+                const float mx = fmax3(mx0, mx2, fmaxf(__uint_as_float(sr[BN - 2]), __uint_as_float(sr[BN - 1])));
+                // Reference maximum.  It moves only when the row maximum grows by
+                // more than kRescaleLog2 (bf16 path: P stays below 2^8, exact
+                // since O and l share the reference); the FP8 path tracks it
+                // exactly so that P <= 1 before the e4m3 scaling.
+                const float m_tile = mx * mult;
+                float m_use = m;
+                if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY) m_use = fmaxf(m, m_tile);
+                if (m_use == -INFINITY) m_use = 0.0f;
                 const float alpha = ex2_approx(m - m_use);
-                const float neg = -m_use;
-                float rsum = 0.0f;
+                const float2 mult2 = make_float2(mult, mult);
+                const float2 neg2 = make_float2(-m_use, -m_use);
+                float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
                 if constexpr (!Cfg::FP8) {
 #pragma unroll
                     for (int c = 0; c < BN / 32; ++c) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int x = 0; x < 16; ++x) {
-                            const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * x], mult, neg));
-                            const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * x + 1], mult, neg));
-                            rsum += p0 + p1;
-                            pk[x] = pack_bf16x2(p0, p1);
+                            const int e = c * 32 + 2 * x;
+                            float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                                  mult2, neg2);
+                            t.x = ex2_approx(t.x);
+                            t.y = ex2_approx(t.y);
+                            if (x & 1) acc1 = __fadd2_rn(acc1, t);
+                            else acc0 = __fadd2_rn(acc0, t);
+                            pk[x] = pack_bf16x2(t.x, t.y);
                         }
                         tmem_st16(s_tmem + c * 16, pk);
                     }
@@ -455,17 +490,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         uint32_t pk[16];
 #pragma unroll
                         for (int x = 0; x < 16; ++x) {
-                            float e[4];
-#pragma unroll
-                            for (int y = 0; y < 4; ++y) {
-                                e[y] = ex2_approx(fmaf(s[c * 64 + 4 * x + y], mult, neg));
-                                rsum += e[y];
-                            }
-                            pk[x] = pack_e4m3x4(e[0] * pv_mult, e[1] * pv_mult, e[2] * pv_mult, e[3] * pv_mult);
+                            const int e = c * 64 + 4 * x;
+                            float2 t0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                                   mult2, neg2);
+                            float2 t1 = __ffma2_rn(
+                                make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), mult2, neg2);
+                            t0.x = ex2_approx(t0.x);
+                            t0.y = ex2_approx(t0.y);
+                            t1.x = ex2_approx(t1.x);
+                            t1.y = ex2_approx(t1.y);
+                            acc0 = __fadd2_rn(acc0, t0);
+                            acc1 = __fadd2_rn(acc1, t1);
+                            pk[x] = pack_e4m3x4(t0.x * pv_mult, t0.y * pv_mult, t1.x * pv_mult, t1.y * pv_mult);
                         }
                         tmem_st16(s_tmem + c * 16, pk);
                     }
                 }
+                const float rsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 l = l * alpha + rsum;
                 // Rescale the accumulator of the rows whose maximum moved.  The
                 // commit that signalled S_t(j) also covers O_t += P_t V_{j-1}, so

@@ -24,9 +24,16 @@ FwdGeometry fwd_geometry() {
 template <class Cfg>
 cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t stream) {
     auto kernel = attn_fwd_kernel<Cfg>;
+    // The register split inside the kernel (setmaxnreg) assumes every thread
+    // is launched with exactly LAUNCH_REGS registers; a different count could
+    // make the increase wait forever, so such a build is refused.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != Cfg::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     // The attribute is per function and per device; setting it is cheap and
     // idempotent, so it is set on every launch (devices may differ per call).
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const long long units = static_cast<long long>(p.n_mblocks) * p.B * p.H;
     kernel<<<dim3(static_cast<unsigned>(units)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream>>>(maps.q, maps.k,

@@ -113,3 +113,31 @@ def test_config3_sweep_sampled_rows(N, d, causal):
     rows = synth.sample_rows(N, 24, seed=N + d)
     e = run_case(B, N, H, d, causal=causal, rows=rows, seed=11)
     assert_bf16_parity(e, f"C3 N={N} d={d} causal={causal}")
+
+
+def _growing_scores(N, H, d, seed):
+    """Scores that grow by ~16 log2-units per 128-key tile for most rows (the
+    running maximum jumps every tile, so the accumulator is rescaled), plus
+    rows whose scores shrink (never rescaled)."""
+    rng = np.random.default_rng(seed)
+    u = np.sign(rng.standard_normal(d))
+    a = rng.uniform(0.25, 1.5, size=(N, H)) * np.where(rng.random((N, H)) < 0.8, 1.0, -1.0)
+    b = np.arange(N)[:, None] / 128.0 + 0.5 * rng.standard_normal((N, H))
+    q = a[None, :, :, None] * u
+    k = b[None, :, :, None] * u + 0.3 * rng.standard_normal((1, N, H, d))
+    v = rng.standard_normal((1, N, H, d))
+    return tuple(synth.to_bf16_bits(x) for x in (q, k, v))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_growing_scores_exercise_rescaling(causal):
+    N, H, d = 1100, 2, 128
+    q, k, v = _growing_scores(N, H, d, seed=3)
+    o, lse = api.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=causal)
+    torch.cuda.synchronize()
+    rows = np.arange(N, dtype=np.int32)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, rows=rows)
+    e = errors(gpu_rows(o, rows), o_ref, lse_rows(lse, rows), lse_ref)
+    # LSE here reaches ~100: the tolerance is relative to its magnitude
+    assert e["rms"] <= 2e-3 and e["max_excess"] <= 1e-2, e
+    assert np.max(np.abs(lse_rows(lse, rows) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))) <= 1e-5, e
