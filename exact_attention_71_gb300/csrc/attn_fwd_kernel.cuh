@@ -97,7 +97,7 @@ struct FwdCfg {
     // MMA warpgroup drops to LOW_REGS and the softmax warpgroups rise to
     // HIGH_REGS.  The sum stays within the launch allocation.
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 248 : (65536 / THREADS) / 8 * 8;
-    static constexpr int LOW_REGS = 72;
+    static constexpr int LOW_REGS = FP8 ? 64 : 88;
     static constexpr int HIGH_REGS_RAW = ((LAUNCH_REGS * THREADS - LOW_REGS * 128) / (NQ * 128)) / 8 * 8;
     static constexpr int HIGH_REGS = HIGH_REGS_RAW > 248 ? 248 : HIGH_REGS_RAW;
     static_assert(HIGH_REGS * NQ * 128 + LOW_REGS * 128 <= LAUNCH_REGS * THREADS, "register split");
@@ -146,6 +146,43 @@ __device__ __forceinline__ void tile_range(const FwdParams& p, int qs, int& lo, 
     const int qe = min(qs + Cfg::BM, p.N) - 1;
     lo = p.window > 0 ? max(0, qs - p.window + 1) / Cfg::BN : 0;
     hi = p.causal ? qe / Cfg::BN : (p.N - 1) / Cfg::BN;
+}
+
+// S_t = Q_t K^T: D / MMA_K instructions, operands in shared memory (both
+// K-major, 128-byte swizzle); each k-step advances the descriptors' start
+// address by a constant.
+template <class Cfg>
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t qdesc, uint64_t kdesc) {
+    constexpr uint32_t fmt = Cfg::FP8 ? 0u : 1u;
+    constexpr uint32_t idesc = make_idesc(fmt, 128, Cfg::BN, 0);
+#pragma unroll
+    for (int kk = 0; kk < Cfg::D / Cfg::MMA_K; ++kk) {
+        constexpr int step_bytes = Cfg::MMA_K * Cfg::ES;
+        const int byte_k = kk * step_bytes;
+        const uint32_t a_off = (byte_k / 128) * (Cfg::BM * 128) + (byte_k % 128);
+        const uint32_t b_off = (byte_k / 128) * (Cfg::BN * 128) + (byte_k % 128);
+        if constexpr (Cfg::FP8)
+            mma_f8_ss(s_tmem, qdesc + (a_off >> 4), kdesc + (b_off >> 4), idesc, kk > 0 ? 1u : 0u);
+        else
+            mma_f16_ss(s_tmem, qdesc + (a_off >> 4), kdesc + (b_off >> 4), idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// O_t (+)= P_t V: BN / MMA_K instructions, P from tensor memory, V from
+// shared memory (MN-major, 128-byte swizzle).
+template <class Cfg>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t vdesc, bool accumulate) {
+    constexpr uint32_t fmt = Cfg::FP8 ? 0u : 1u;
+    constexpr uint32_t idesc = make_idesc(fmt, 128, Cfg::D, 1);
+    const uint32_t acc0 = accumulate ? 1u : 0u;
+#pragma unroll
+    for (int kk = 0; kk < Cfg::BN / Cfg::MMA_K; ++kk) {
+        const uint64_t off = (static_cast<uint64_t>(kk) * Cfg::MMA_K * 128) >> 4;
+        if constexpr (Cfg::FP8)
+            mma_f8_ts(o_tmem, p_tmem + kk * (Cfg::MMA_K / 4), vdesc + off, idesc, kk > 0 ? 1u : acc0);
+        else
+            mma_f16_ts(o_tmem, p_tmem + kk * (Cfg::MMA_K / 2), vdesc + off, idesc, kk > 0 ? 1u : acc0);
+    }
 }
 
 template <class Cfg>
@@ -274,37 +311,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (warp == Cfg::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t fmt = Cfg::FP8 ? 0u : 1u;
-            constexpr uint32_t idesc_s = make_idesc(fmt, 128, BN, 0);
-            constexpr uint32_t idesc_o = make_idesc(fmt, 128, D, 1);
             const uint32_t sQ_addr = smem_u32(sQ);
             const uint32_t sKV_addr = smem_u32(sKV);
             bool ok = true;
 #pragma unroll
             for (int t = 0; t < NQ; ++t)
                 if (active[t] && ok) ok = wait_phase(&bars->q_full[t], 0, abort_flag, p, SITE_MMA_Q);
+            // Descriptor bases; each k-step adds a compile-time offset.
+            uint64_t qdesc[NQ];
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) qdesc[t] = sdesc_sw128(sQ_addr + t * Cfg::Q_TILE_BYTES, 16, 1024);
             uint32_t it = 0;
             uint32_t pv_count[NQ];
 #pragma unroll
             for (int t = 0; t < NQ; ++t) pv_count[t] = 0;
             uint32_t prev_v_stage = 0, prev_v_round = 0;
-
-            auto issue_pv = [&](int t, int j, uint32_t vstage) {
-                const uint32_t v_base = sKV_addr + vstage * Cfg::KV_TILE_BYTES;
-                const uint32_t p_tmem = tmem + t * Cfg::S_COL;
-                const uint32_t o_tmem = tmem + Cfg::O_COL0 + t * D;
-#pragma unroll
-                for (int kk = 0; kk < BN / Cfg::MMA_K; ++kk) {
-                    const uint64_t bdesc = sdesc_sw128(v_base + kk * Cfg::MMA_K * 128, BN * 128, 1024);
-                    const uint32_t acc = (pv_count[t] > 0 || kk > 0) ? 1u : 0u;
-                    if constexpr (Cfg::FP8)
-                        mma_f8_ts(o_tmem, p_tmem + kk * (Cfg::MMA_K / 4), bdesc, idesc_o, acc);
-                    else
-                        mma_f16_ts(o_tmem, p_tmem + kk * (Cfg::MMA_K / 2), bdesc, idesc_o, acc);
-                }
-                ++pv_count[t];
-                if (j == hi[t]) mma_commit(&bars->o_full[t]);
-            };
 
             for (int u = u_lo; u <= u_hi && ok; ++u) {
                 const uint32_t kstage = it % NSTAGE, kround = it / NSTAGE;
@@ -316,6 +337,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
+                const uint64_t kdesc = sdesc_sw128(sKV_addr + kstage * Cfg::KV_TILE_BYTES, 16, 1024);
+                const uint64_t vdesc_prev = sdesc_sw128(sKV_addr + prev_v_stage * Cfg::KV_TILE_BYTES, BN * 128, 1024);
                 bool v_ready = false;
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
@@ -334,24 +357,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        issue_pv(t, u - 1, prev_v_stage);
+                        issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev,
+                                      pv_count[t] > 0);
+                        ++pv_count[t];
+                        if (u - 1 == hi[t]) mma_commit(&bars->o_full[t]);
                     }
                     if (u >= lo[t] && u <= hi[t]) {
-                        const uint32_t q_base = sQ_addr + t * Cfg::Q_TILE_BYTES;
-                        const uint32_t k_base = sKV_addr + kstage * Cfg::KV_TILE_BYTES;
-                        const uint32_t s_tmem = tmem + t * Cfg::S_COL;
-#pragma unroll
-                        for (int kk = 0; kk < D / Cfg::MMA_K; ++kk) {
-                            const int byte_k = kk * Cfg::MMA_K * Cfg::ES;
-                            const uint32_t a_off = (byte_k / 128) * (BM * 128) + (byte_k % 128);
-                            const uint32_t b_off = (byte_k / 128) * (BN * 128) + (byte_k % 128);
-                            const uint64_t adesc = sdesc_sw128(q_base + a_off, 16, 1024);
-                            const uint64_t bdesc = sdesc_sw128(k_base + b_off, 16, 1024);
-                            if constexpr (Cfg::FP8)
-                                mma_f8_ss(s_tmem, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-                            else
-                                mma_f16_ss(s_tmem, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-                        }
+                        issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
                         mma_commit(&bars->s_full[t]);
                     }
                 }
@@ -364,15 +376,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (ok) {
                 // P V of the last key tile.
                 ok = wait_phase(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p, SITE_MMA_FULL);
+                const uint64_t vdesc_prev = sdesc_sw128(sKV_addr + prev_v_stage * Cfg::KV_TILE_BYTES, BN * 128, 1024);
 #pragma unroll
-                for (int t = 0; t < NQ && ok; ++t) {
-                    if (!active[t] || u_hi < lo[t] || u_hi > hi[t]) continue;
+                for (int t = 0; t < NQ; ++t) {
+                    if (!ok || !active[t] || u_hi < lo[t] || u_hi > hi[t]) continue;
                     if (!wait_phase(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
                         ok = false;
-                        break;
+                        continue;
                     }
                     tc_fence_after();
-                    issue_pv(t, u_hi, prev_v_stage);
+                    issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev, pv_count[t] > 0);
+                    ++pv_count[t];
+                    mma_commit(&bars->o_full[t]);
                 }
                 if (ok) mma_commit(&bars->ring_empty[prev_v_stage]);
             }
@@ -411,9 +426,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         float m = -INFINITY;   // running max of the log2-scaled scores
         float l = 0.0f;        // running sum of exp2(score - m)
         uint32_t count = 0;
-        bool ok = active[t];
+        int my_lo, my_hi;
+        tile_range<Cfg>(p, qs, my_lo, my_hi);
+        bool ok = qs < p.N;
         if (ok) {
-            for (int j = lo[t]; j <= hi[t]; ++j) {
+            for (int j = my_lo; j <= my_hi; ++j) {
                 bool w = wait_phase(&bars->s_full[t], count & 1, abort_flag, p, SITE_SOFTMAX_S);
                 if (!__all_sync(0xffffffffu, w)) {
                     ok = false;
