@@ -141,6 +141,14 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
     }
 }
 
+// wait_phase for a converged warp: every lane polls; the result is the same
+// in every lane (a lane that gave up makes the whole warp give up).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          const FwdParams& p, int site) {
+    const bool w = wait_phase(bar, parity, abort_flag, p, site);
+    return __all_sync(0xffffffffu, w);
+}
+
 template <class Cfg>
 __device__ __forceinline__ void tile_range(const FwdParams& p, int qs, int& lo, int& hi) {
     const int qe = min(qs + Cfg::BM, p.N) - 1;
@@ -310,14 +318,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         __syncwarp();
     } else if (warp == Cfg::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (waits, descriptor arithmetic) so the
+        // descriptors stay warp-uniform; one elected lane issues the MMAs and
+        // their commits (a commit tracks the MMAs of the issuing thread).
+        {
             const uint32_t sQ_addr = smem_u32(sQ);
             const uint32_t sKV_addr = smem_u32(sKV);
             bool ok = true;
 #pragma unroll
             for (int t = 0; t < NQ; ++t)
-                if (active[t] && ok) ok = wait_phase(&bars->q_full[t], 0, abort_flag, p, SITE_MMA_Q);
-            // Descriptor bases; each k-step adds a compile-time offset.
+                if (active[t] && ok) ok = warp_wait(&bars->q_full[t], 0, abort_flag, p, SITE_MMA_Q);
             uint64_t qdesc[NQ];
 #pragma unroll
             for (int t = 0; t < NQ; ++t) qdesc[t] = sdesc_sw128(sQ_addr + t * Cfg::Q_TILE_BYTES, 16, 1024);
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 ++it;
                 const uint32_t vstage = it % NSTAGE, vround = it / NSTAGE;
                 ++it;
-                if (!wait_phase(&bars->ring_full[kstage], kround & 1, abort_flag, p, SITE_MMA_FULL)) {
+                if (!warp_wait(&bars->ring_full[kstage], kround & 1, abort_flag, p, SITE_MMA_FULL)) {
                     ok = false;
                     break;
                 }
@@ -345,55 +355,71 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (!active[t]) continue;
                     if (u > u_lo && u - 1 >= lo[t] && u - 1 <= hi[t]) {
                         if (!v_ready) {
-                            if (!wait_phase(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p,
-                                            SITE_MMA_FULL)) {
+                            if (!warp_wait(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p,
+                                           SITE_MMA_FULL)) {
                                 ok = false;
                                 break;
                             }
                             v_ready = true;
                         }
-                        if (!wait_phase(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
+                        if (!warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev,
-                                      pv_count[t] > 0);
+                        if (elect_one()) {
+                            issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev,
+                                          pv_count[t] > 0);
+                            if (u - 1 == hi[t]) mma_commit(&bars->o_full[t]);
+                        }
+                        __syncwarp();
                         ++pv_count[t];
-                        if (u - 1 == hi[t]) mma_commit(&bars->o_full[t]);
                     }
                     if (u >= lo[t] && u <= hi[t]) {
-                        issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
-                        mma_commit(&bars->s_full[t]);
+                        if (elect_one()) {
+                            issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
+                            mma_commit(&bars->s_full[t]);
+                        }
+                        __syncwarp();
                     }
                 }
                 if (!ok) break;
-                mma_commit(&bars->ring_empty[kstage]);
-                if (u > u_lo) mma_commit(&bars->ring_empty[prev_v_stage]);
+                if (elect_one()) {
+                    mma_commit(&bars->ring_empty[kstage]);
+                    if (u > u_lo) mma_commit(&bars->ring_empty[prev_v_stage]);
+                }
+                __syncwarp();
                 prev_v_stage = vstage;
                 prev_v_round = vround;
             }
             if (ok) {
                 // P V of the last key tile.
-                ok = wait_phase(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p, SITE_MMA_FULL);
+                ok = warp_wait(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p, SITE_MMA_FULL);
                 const uint64_t vdesc_prev = sdesc_sw128(sKV_addr + prev_v_stage * Cfg::KV_TILE_BYTES, BN * 128, 1024);
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
                     if (!ok || !active[t] || u_hi < lo[t] || u_hi > hi[t]) continue;
-                    if (!wait_phase(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
+                    if (!warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
                         ok = false;
                         continue;
                     }
                     tc_fence_after();
-                    issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev, pv_count[t] > 0);
+                    if (elect_one()) {
+                        issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev,
+                                      pv_count[t] > 0);
+                        mma_commit(&bars->o_full[t]);
+                    }
+                    __syncwarp();
                     ++pv_count[t];
-                    mma_commit(&bars->o_full[t]);
                 }
-                if (ok) mma_commit(&bars->ring_empty[prev_v_stage]);
+                if (ok && elect_one()) mma_commit(&bars->ring_empty[prev_v_stage]);
+                __syncwarp();
             }
-            // Every MMA this thread issued has finished before teardown.
-            mma_commit(&bars->drain);
-            wait_phase(&bars->drain, 0, abort_flag, p, SITE_MMA_DRAIN);
+            // Every MMA the elected lane issued has finished before teardown.
+            if (elect_one()) {
+                mma_commit(&bars->drain);
+                wait_phase(&bars->drain, 0, abort_flag, p, SITE_MMA_DRAIN);
+            }
         }
         __syncwarp();
     }
