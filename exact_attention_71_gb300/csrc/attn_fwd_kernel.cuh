@@ -149,6 +149,23 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, w);
 }
 
+// Teardown wait for the CTA's own asynchronous work (TMA copies it issued,
+// MMAs it committed).  That work always completes, so this wait ignores the
+// abort flag and uses at least kDrainCycles even when the per-wait limit has
+// been made small, so that no CTA exits with copies or MMAs in flight.
+constexpr unsigned long long kDrainCycles = 2000000000ull;
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity, const FwdParams& p, int site) {
+    const unsigned long long lim = p.wait_limit > kDrainCycles ? p.wait_limit : kDrainCycles;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (static_cast<unsigned long long>(clock64() - t0) > lim) {
+            atomicCAS(p.status, 0, site);
+            return false;
+        }
+    }
+    return true;
+}
+
 template <class Cfg>
 __device__ __forceinline__ void tile_range(const FwdParams& p, int qs, int& lo, int& hi) {
     const int qe = min(qs + Cfg::BM, p.N) - 1;
@@ -303,16 +320,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ++it;
                 }
             }
-            if (!ok) {
-                // Let copies already in flight land before the CTA exits.
+            // Let every copy this warp issued land before the CTA can exit (on
+            // the normal path these phases have completed already).
+            {
                 const uint32_t first = it > NSTAGE ? it - NSTAGE : 0;
-                for (uint32_t k = first; k < it; ++k) {
-                    const uint32_t stage = k % NSTAGE, round = k / NSTAGE;
-                    const long long t0 = clock64();
-                    while (!mbar_try_wait(&bars->ring_full[stage], round & 1) &&
-                           static_cast<unsigned long long>(clock64() - t0) <= p.wait_limit) {
-                    }
-                }
+                for (uint32_t k = first; k < it; ++k)
+                    drain_wait(&bars->ring_full[k % NSTAGE], (k / NSTAGE) & 1, p, SITE_LOAD_DRAIN);
+#pragma unroll
+                for (int t = 0; t < NQ; ++t)
+                    if (active[t]) drain_wait(&bars->q_full[t], 0, p, SITE_LOAD_DRAIN);
             }
         }
         __syncwarp();
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // Every MMA the elected lane issued has finished before teardown.
             if (elect_one()) {
                 mma_commit(&bars->drain);
-                wait_phase(&bars->drain, 0, abort_flag, p, SITE_MMA_DRAIN);
+                drain_wait(&bars->drain, 0, p, SITE_MMA_DRAIN);
             }
         }
         __syncwarp();
