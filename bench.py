@@ -290,12 +290,18 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(device)
 
+    # Multi-rank: the global batch is B x world; each rank owns a contiguous
+    # shard of it (no data exchange between ranks).
+    from exact_attention_71_gb300.shard import batch_shard
+    b_start, b_stop = batch_shard(w["B"] * ws, ws, rank)
+    global_batch = w["B"] * ws
+    w = dict(w, B=b_stop - b_start)
     # Two resident input sets (> L2 each) used alternately, so no step finds
     # the previous step's inputs in the 129 MB L2.
     sets = []
     arrs0 = None
     for s in range(2):
-        (q, k, v), arrs = make_inputs(w, device, seed=s)
+        (q, k, v), arrs = make_inputs(w, device, seed=s + 2 * b_start)
         if s == 0:
             arrs0 = arrs
         if w["dtype"] == "fp8":
@@ -359,7 +365,8 @@ def main():
                        "window": w["window"], "flops_per_step": flops,
                        "flop_convention": "4 B H N^2 d, halved for causal; window: 4 d x attended pairs",
                        "l2": "inputs larger than L2 (two resident input sets, alternated per step)",
-                       "parallelism": f"independent replicas x{ws}"},
+                       "global_batch": global_batch,
+                       "parallelism": f"batch shards x{ws}, no collective on the data path"},
             "roofline": roof, "gpu_launches": args.steps, "clocks": clk.summary() if rank == 0 else None}
 
     if not args.quick and rank == 0:
