@@ -59,6 +59,25 @@ int status_ptr(int** out) {
     return ATTN_OK;
 }
 
+int g_sm_count[kMaxDevices] = {};
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count(int* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(multiProcessorCount)");
+        g_sm_count[dev] = n > 0 ? n : 1;
+    }
+    *out = g_sm_count[dev];
+    return ATTN_OK;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -119,7 +138,7 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
                    int d, int causal, float scale, int window, const float* qs, const float* ks, const float* vs,
                    void* stream) {
     attn::FwdGeometry g;
-    cudaError_t (*run)(const attn::FwdMaps&, const attn::FwdParams&, cudaStream_t) = nullptr;
+    cudaError_t (*run)(const attn::FwdMaps&, const attn::FwdParams&, int, cudaStream_t) = nullptr;
     if (fp8) {
         if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 only (got %d)", d);
         g = attn::geom_fp8_d128();
@@ -154,7 +173,9 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
     p.n_mblocks = (N + g.nq * 128 - 1) / (g.nq * 128);
     p.wait_limit = g_wait_limit.load();
     if ((rc = status_ptr(&p.status)) != ATTN_OK) return rc;
-    cudaError_t e = run(maps, p, static_cast<cudaStream_t>(stream));
+    int sms = 0;
+    if ((rc = sm_count(&sms)) != ATTN_OK) return rc;
+    cudaError_t e = run(maps, p, sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd launch");
     return ATTN_OK;
 }

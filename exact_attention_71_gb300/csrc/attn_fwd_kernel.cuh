@@ -97,7 +97,7 @@ struct FwdCfg {
     // MMA warpgroup drops to LOW_REGS and the softmax warpgroups rise to
     // HIGH_REGS.  The sum stays within the launch allocation.
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 248 : (65536 / THREADS) / 8 * 8;
-    static constexpr int LOW_REGS = FP8 ? 64 : 88;
+    static constexpr int LOW_REGS = FP8 ? 72 : 112;
     static constexpr int HIGH_REGS_RAW = ((LAUNCH_REGS * THREADS - LOW_REGS * 128) / (NQ * 128)) / 8 * 8;
     static constexpr int HIGH_REGS = HIGH_REGS_RAW > 248 ? 248 : HIGH_REGS_RAW;
     static_assert(HIGH_REGS * NQ * 128 + LOW_REGS * 128 <= LAUNCH_REGS * THREADS, "register split");
@@ -113,6 +113,7 @@ struct FwdCfg {
 
 struct SharedBarriers {
     uint64_t q_full[2];
+    uint64_t q_empty[2];
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_full[2];
@@ -173,6 +174,61 @@ __device__ __forceinline__ void tile_range(const FwdParams& p, int qs, int& lo, 
     hi = p.causal ? qe / Cfg::BN : (p.N - 1) / Cfg::BN;
 }
 
+// Work items are (query block of NQ*128 rows, batch*head).  Causal items
+// are numbered heaviest query block first, non-causal items head by head so
+// that the CTAs running together share K and V in L2.  CTA c takes, in round
+// m, item m*G + c when m is even and m*G + G-1-c when m is odd (G = grid):
+// the zigzag gives the CTA that got the lightest item of one round the
+// heaviest of the next, which balances causal work without any scheduler
+// state in memory.
+__device__ __forceinline__ int round_item(int m) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    return m * G + ((m & 1) ? (G - 1 - c) : c);
+}
+
+__device__ __forceinline__ void item_coords(const FwdParams& p, int item, int& mb, int& bh) {
+    const int BH = p.B * p.H;
+    if (p.causal) {
+        mb = p.n_mblocks - 1 - item / BH;
+        bh = item % BH;
+    } else {
+        mb = item % p.n_mblocks;
+        bh = item / p.n_mblocks;
+    }
+}
+
+template <int NQ>
+struct WorkItem {
+    int b, h, bh, q0;
+    int lo[NQ], hi[NQ];
+    bool active[NQ];
+    int u_lo, u_hi;       // union of the active tiles' key-tile ranges
+};
+
+template <class Cfg>
+__device__ __forceinline__ WorkItem<Cfg::NQ> decode_item(const FwdParams& p, int item) {
+    WorkItem<Cfg::NQ> w;
+    int mb;
+    item_coords(p, item, mb, w.bh);
+    w.b = w.bh / p.H;
+    w.h = w.bh % p.H;
+    w.q0 = mb * Cfg::NQ * Cfg::BM;
+#pragma unroll
+    for (int t = 0; t < Cfg::NQ; ++t) {
+        w.active[t] = (w.q0 + t * Cfg::BM) < p.N;
+        tile_range<Cfg>(p, w.q0 + t * Cfg::BM, w.lo[t], w.hi[t]);
+    }
+    w.u_lo = w.lo[0];
+    w.u_hi = w.hi[0];
+#pragma unroll
+    for (int t = 1; t < Cfg::NQ; ++t)
+        if (w.active[t]) {
+            w.u_lo = min(w.u_lo, w.lo[t]);
+            w.u_hi = max(w.u_hi, w.hi[t]);
+        }
+    return w;
+}
+
 // S_t = Q_t K^T: D / MMA_K instructions, operands in shared memory (both
 // K-major, 128-byte swizzle); each k-step advances the descriptors' start
 // address by a constant.
@@ -226,37 +282,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Work item: heaviest query blocks first when causal.
-    const int BH = p.B * p.H;
-    int mb, bh;
-    if (p.causal) {
-        mb = p.n_mblocks - 1 - static_cast<int>(blockIdx.x / BH);
-        bh = static_cast<int>(blockIdx.x % BH);
-    } else {
-        mb = static_cast<int>(blockIdx.x % p.n_mblocks);
-        bh = static_cast<int>(blockIdx.x / p.n_mblocks);
-    }
-    const int b = bh / p.H, h = bh % p.H;
-    const int q0 = mb * NQ * BM;
-
-    int lo[NQ], hi[NQ];
-    bool active[NQ];
-#pragma unroll
-    for (int t = 0; t < NQ; ++t) {
-        active[t] = (q0 + t * BM) < p.N;
-        tile_range<Cfg>(p, q0 + t * BM, lo[t], hi[t]);
-    }
-    int u_lo = lo[0], u_hi = hi[0];
-#pragma unroll
-    for (int t = 1; t < NQ; ++t)
-        if (active[t]) {
-            u_lo = min(u_lo, lo[t]);
-            u_hi = max(u_hi, hi[t]);
-        }
-
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->q_full[t], 1);
+            mbar_init(&bars->q_empty[t], 1);
             mbar_init(&bars->s_full[t], 1);
             mbar_init(&bars->p_full[t], 128);
             mbar_init(&bars->o_full[t], 1);
@@ -283,6 +312,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    const int total_items = p.n_mblocks * p.B * p.H;
 
     if (warp >= 4 * NQ) {
     regs_decrease<Cfg::LOW_REGS>();
@@ -291,45 +321,58 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (lane == 0) {
             const uint64_t pol_q = l2_policy_evict_first();
             const uint64_t pol_kv = l2_policy_evict_last();
-#pragma unroll
-            for (int t = 0; t < NQ; ++t) {
-                if (!active[t]) continue;
-                mbar_arrive_expect_tx(&bars->q_full[t], Cfg::Q_TILE_BYTES);
-#pragma unroll
-                for (int cb = 0; cb < Cfg::NCB; ++cb)
-                    tma_load_4d(sQ + t * Cfg::Q_TILE_BYTES + cb * (BM * 128), &tmap_q, &bars->q_full[t],
-                                cb * Cfg::BOX_ELEMS, h, q0 + t * BM, b, pol_q);
-            }
             uint32_t it = 0;
-            bool ok = true;
-            for (int j = u_lo; j <= u_hi && ok; ++j) {
+            uint32_t qn[NQ];
 #pragma unroll
-                for (int kind = 0; kind < 2; ++kind) {
-                    const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
-                    if (!wait_phase(&bars->ring_empty[stage], (round & 1) ^ 1, abort_flag, p, SITE_LOAD_EMPTY)) {
+            for (int t = 0; t < NQ; ++t) qn[t] = 0;
+            bool ok = true;
+            for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
+            const int item = round_item(rnd);
+            if (item >= total_items) continue;
+                const WorkItem<NQ> w = decode_item<Cfg>(p, item);
+#pragma unroll
+                for (int t = 0; t < NQ; ++t) {
+                    if (!w.active[t] || !ok) continue;
+                    // The previous item's S MMAs of this tile must be done.
+                    if (!wait_phase(&bars->q_empty[t], (qn[t] & 1) ^ 1, abort_flag, p, SITE_LOAD_EMPTY)) {
                         ok = false;
-                        break;
+                        continue;
                     }
-                    mbar_arrive_expect_tx(&bars->ring_full[stage], Cfg::KV_TILE_BYTES);
-                    uint8_t* dst = sKV + stage * Cfg::KV_TILE_BYTES;
-                    const CUtensorMap* map = kind == 0 ? &tmap_k : &tmap_v;
+                    ++qn[t];
+                    mbar_arrive_expect_tx(&bars->q_full[t], Cfg::Q_TILE_BYTES);
 #pragma unroll
                     for (int cb = 0; cb < Cfg::NCB; ++cb)
-                        tma_load_4d(dst + cb * (BN * 128), map, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS, h,
-                                    j * BN, b, pol_kv);
-                    ++it;
+                        tma_load_4d(sQ + t * Cfg::Q_TILE_BYTES + cb * (BM * 128), &tmap_q, &bars->q_full[t],
+                                    cb * Cfg::BOX_ELEMS, w.h, w.q0 + t * BM, w.b, pol_q);
+                }
+                for (int j = w.u_lo; j <= w.u_hi && ok; ++j) {
+#pragma unroll
+                    for (int kind = 0; kind < 2; ++kind) {
+                        const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
+                        if (!wait_phase(&bars->ring_empty[stage], (round & 1) ^ 1, abort_flag, p,
+                                        SITE_LOAD_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars->ring_full[stage], Cfg::KV_TILE_BYTES);
+                        uint8_t* dst = sKV + stage * Cfg::KV_TILE_BYTES;
+                        const CUtensorMap* map = kind == 0 ? &tmap_k : &tmap_v;
+#pragma unroll
+                        for (int cb = 0; cb < Cfg::NCB; ++cb)
+                            tma_load_4d(dst + cb * (BN * 128), map, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS,
+                                        w.h, j * BN, w.b, pol_kv);
+                        ++it;
+                    }
                 }
             }
             // Let every copy this warp issued land before the CTA can exit (on
             // the normal path these phases have completed already).
-            {
-                const uint32_t first = it > NSTAGE ? it - NSTAGE : 0;
-                for (uint32_t k = first; k < it; ++k)
-                    drain_wait(&bars->ring_full[k % NSTAGE], (k / NSTAGE) & 1, p, SITE_LOAD_DRAIN);
+            const uint32_t first = it > NSTAGE ? it - NSTAGE : 0;
+            for (uint32_t k = first; k < it; ++k)
+                drain_wait(&bars->ring_full[k % NSTAGE], (k / NSTAGE) & 1, p, SITE_LOAD_DRAIN);
 #pragma unroll
-                for (int t = 0; t < NQ; ++t)
-                    if (active[t]) drain_wait(&bars->q_full[t], 0, p, SITE_LOAD_DRAIN);
-            }
+            for (int t = 0; t < NQ; ++t)
+                if (qn[t] > 0) drain_wait(&bars->q_full[t], (qn[t] - 1) & 1, p, SITE_LOAD_DRAIN);
         }
         __syncwarp();
     } else if (warp == Cfg::MMA_WARP) {
@@ -337,23 +380,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // The whole warp runs the loop (waits, descriptor arithmetic) so the
         // descriptors stay warp-uniform; one elected lane issues the MMAs and
         // their commits (a commit tracks the MMAs of the issuing thread).
-        {
-            const uint32_t sQ_addr = smem_u32(sQ);
-            const uint32_t sKV_addr = smem_u32(sKV);
-            bool ok = true;
+        const uint32_t sQ_addr = smem_u32(sQ);
+        const uint32_t sKV_addr = smem_u32(sKV);
+        uint64_t qdesc[NQ];
 #pragma unroll
-            for (int t = 0; t < NQ; ++t)
-                if (active[t] && ok) ok = warp_wait(&bars->q_full[t], 0, abort_flag, p, SITE_MMA_Q);
-            uint64_t qdesc[NQ];
+        for (int t = 0; t < NQ; ++t) qdesc[t] = sdesc_sw128(sQ_addr + t * Cfg::Q_TILE_BYTES, 16, 1024);
+        uint32_t it = 0;
+        uint32_t pv_count[NQ], qn[NQ];
 #pragma unroll
-            for (int t = 0; t < NQ; ++t) qdesc[t] = sdesc_sw128(sQ_addr + t * Cfg::Q_TILE_BYTES, 16, 1024);
-            uint32_t it = 0;
-            uint32_t pv_count[NQ];
+        for (int t = 0; t < NQ; ++t) pv_count[t] = qn[t] = 0;
+        bool ok = true;
+        for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
+            const int item = round_item(rnd);
+            if (item >= total_items) continue;
+            const WorkItem<NQ> w = decode_item<Cfg>(p, item);
+            bool item_first_pv[NQ];
 #pragma unroll
-            for (int t = 0; t < NQ; ++t) pv_count[t] = 0;
+            for (int t = 0; t < NQ; ++t) {
+                item_first_pv[t] = true;
+                if (w.active[t] && ok) {
+                    ok = warp_wait(&bars->q_full[t], qn[t] & 1, abort_flag, p, SITE_MMA_Q);
+                    ++qn[t];
+                }
+            }
             uint32_t prev_v_stage = 0, prev_v_round = 0;
-
-            for (int u = u_lo; u <= u_hi && ok; ++u) {
+            for (int u = w.u_lo; u <= w.u_hi && ok; ++u) {
                 const uint32_t kstage = it % NSTAGE, kround = it / NSTAGE;
                 ++it;
                 const uint32_t vstage = it % NSTAGE, vround = it / NSTAGE;
@@ -368,8 +419,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 bool v_ready = false;
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
-                    if (!active[t]) continue;
-                    if (u > u_lo && u - 1 >= lo[t] && u - 1 <= hi[t]) {
+                    if (!w.active[t]) continue;
+                    if (u > w.u_lo && u - 1 >= w.lo[t] && u - 1 <= w.hi[t]) {
                         if (!v_ready) {
                             if (!warp_wait(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p,
                                            SITE_MMA_FULL)) {
@@ -385,16 +436,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tc_fence_after();
                         if (elect_one()) {
                             issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev,
-                                          pv_count[t] > 0);
-                            if (u - 1 == hi[t]) mma_commit(&bars->o_full[t]);
+                                          !item_first_pv[t]);
+                            if (u - 1 == w.hi[t]) mma_commit(&bars->o_full[t]);
                         }
                         __syncwarp();
+                        item_first_pv[t] = false;
                         ++pv_count[t];
                     }
-                    if (u >= lo[t] && u <= hi[t]) {
+                    if (u >= w.lo[t] && u <= w.hi[t]) {
                         if (elect_one()) {
                             issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
                             mma_commit(&bars->s_full[t]);
+                            // Q_t is free for the next item once its last S MMA is done.
+                            if (u == w.hi[t]) mma_commit(&bars->q_empty[t]);
                         }
                         __syncwarp();
                     }
@@ -402,40 +456,39 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (!ok) break;
                 if (elect_one()) {
                     mma_commit(&bars->ring_empty[kstage]);
-                    if (u > u_lo) mma_commit(&bars->ring_empty[prev_v_stage]);
+                    if (u > w.u_lo) mma_commit(&bars->ring_empty[prev_v_stage]);
                 }
                 __syncwarp();
                 prev_v_stage = vstage;
                 prev_v_round = vround;
             }
-            if (ok) {
-                // P V of the last key tile.
-                ok = warp_wait(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p, SITE_MMA_FULL);
-                const uint64_t vdesc_prev = sdesc_sw128(sKV_addr + prev_v_stage * Cfg::KV_TILE_BYTES, BN * 128, 1024);
+            if (!ok) break;
+            // P V of the item's last key tile.
+            ok = warp_wait(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p, SITE_MMA_FULL);
+            const uint64_t vdesc_prev = sdesc_sw128(sKV_addr + prev_v_stage * Cfg::KV_TILE_BYTES, BN * 128, 1024);
 #pragma unroll
-                for (int t = 0; t < NQ; ++t) {
-                    if (!ok || !active[t] || u_hi < lo[t] || u_hi > hi[t]) continue;
-                    if (!warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
-                        ok = false;
-                        continue;
-                    }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev,
-                                      pv_count[t] > 0);
-                        mma_commit(&bars->o_full[t]);
-                    }
-                    __syncwarp();
-                    ++pv_count[t];
+            for (int t = 0; t < NQ; ++t) {
+                if (!ok || !w.active[t] || w.u_hi < w.lo[t] || w.u_hi > w.hi[t]) continue;
+                if (!warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
+                    ok = false;
+                    continue;
                 }
-                if (ok && elect_one()) mma_commit(&bars->ring_empty[prev_v_stage]);
+                tc_fence_after();
+                if (elect_one()) {
+                    issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev, !item_first_pv[t]);
+                    mma_commit(&bars->o_full[t]);
+                }
                 __syncwarp();
+                item_first_pv[t] = false;
+                ++pv_count[t];
             }
-            // Every MMA the elected lane issued has finished before teardown.
-            if (elect_one()) {
-                mma_commit(&bars->drain);
-                drain_wait(&bars->drain, 0, p, SITE_MMA_DRAIN);
-            }
+            if (ok && elect_one()) mma_commit(&bars->ring_empty[prev_v_stage]);
+            __syncwarp();
+        }
+        // Every MMA the elected lane issued has finished before teardown.
+        if (elect_one()) {
+            mma_commit(&bars->drain);
+            drain_wait(&bars->drain, 0, p, SITE_MMA_DRAIN);
         }
         __syncwarp();
     }
@@ -445,36 +498,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int t = warp >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
-        const int qs = q0 + t * BM;
-        const int i = qs + r;                                  // query row
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + t * Cfg::S_COL;
         const uint32_t o_tmem = tmem + lane_off + Cfg::O_COL0 + t * D;
-        // Visible keys of row i: [klo, khi].
-        const int klo = p.window > 0 ? i - p.window + 1 : 0;
-        const int khi = p.causal ? min(i, p.N - 1) : p.N - 1;
         const int nblk = (p.N + 127) / 128;
-
-        float vmax = 1.0f;
-        float q_mult = p.scale_log2;
-        if constexpr (Cfg::FP8) {
-            const float* vs = p.v_scale + static_cast<size_t>(bh) * nblk;
-            vmax = 0.0f;
-            for (int x = 0; x < nblk; ++x) vmax = fmaxf(vmax, vs[x]);
-            if (!(vmax > 0.0f)) vmax = 1.0f;
-            q_mult *= p.q_scale[static_cast<size_t>(bh) * nblk + qs / 128];
-        }
-
-        float m = -INFINITY;   // running max of the log2-scaled scores
-        float l = 0.0f;        // running sum of exp2(score - m)
-        uint32_t count = 0;
-        int my_lo, my_hi;
-        tile_range<Cfg>(p, qs, my_lo, my_hi);
-        bool ok = qs < p.N;
-        if (ok) {
+        uint32_t count = 0;    // S tiles consumed (s_full phases)
+        uint32_t qn = 0;       // items in which this tile was active (o_full phases)
+        bool ok = true;
+        for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
+            const int item = round_item(rnd);
+            if (item >= total_items) continue;
+            int mb, bh;
+            item_coords(p, item, mb, bh);
+            const int b = bh / p.H, h = bh % p.H;
+            const int qs = mb * NQ * BM + t * BM;
+            if (qs >= p.N) continue;                         // tile t inactive for this item
+            const int i = qs + r;                                  // query row
+            // Visible keys of row i: [klo, khi].
+            const int klo = p.window > 0 ? i - p.window + 1 : 0;
+            const int khi = p.causal ? min(i, p.N - 1) : p.N - 1;
+            float vmax = 1.0f;
+            float q_mult = p.scale_log2;
+            if constexpr (Cfg::FP8) {
+                const float* vs = p.v_scale + static_cast<size_t>(bh) * nblk;
+                vmax = 0.0f;
+                for (int x = 0; x < nblk; ++x) vmax = fmaxf(vmax, vs[x]);
+                if (!(vmax > 0.0f)) vmax = 1.0f;
+                q_mult *= p.q_scale[static_cast<size_t>(bh) * nblk + qs / 128];
+            }
+            float m = -INFINITY;   // reference maximum of the log2-scaled scores
+            float l = 0.0f;        // running sum of exp2(score - m)
+            int my_lo, my_hi;
+            tile_range<Cfg>(p, qs, my_lo, my_hi);
             for (int j = my_lo; j <= my_hi; ++j) {
-                bool w = wait_phase(&bars->s_full[t], count & 1, abort_flag, p, SITE_SOFTMAX_S);
-                if (!__all_sync(0xffffffffu, w)) {
+                bool wt = wait_phase(&bars->s_full[t], count & 1, abort_flag, p, SITE_SOFTMAX_S);
+                if (!__all_sync(0xffffffffu, wt)) {
                     ok = false;
                     break;
                 }
@@ -570,7 +628,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // Rescale the accumulator of the rows whose maximum moved.  The
                 // commit that signalled S_t(j) also covers O_t += P_t V_{j-1}, so
                 // O_t is stable here; the next P V waits for p_full below.
-                if (count > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                if (j > my_lo && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t orr[32];
@@ -588,37 +646,38 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 m = m_use;
                 ++count;
             }
-        }
-        if (ok) {
-            bool w = wait_phase(&bars->o_full[t], 0, abort_flag, p, SITE_SOFTMAX_O);
-            ok = __all_sync(0xffffffffu, w);
-        }
-        if (ok) {
-            tc_fence_after();
-            float out_mult = 1.0f / l;
-            if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / 256.0f);
-            const bool store = i < p.N;
-            __nv_bfloat16* orow =
-                reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * p.N + i) * p.H + h) * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t orr[32];
-                tmem_ld32(o_tmem + c * 32, orr);
-                tmem_wait_ld();
-                reg_fence32(orr);
-                uint32_t pk[16];
-#pragma unroll
-                for (int x = 0; x < 16; ++x)
-                    pk[x] = pack_bf16x2(__uint_as_float(orr[2 * x]) * out_mult,
-                                        __uint_as_float(orr[2 * x + 1]) * out_mult);
-                if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
-                }
+            if (!ok) break;
+            {
+                bool wt = wait_phase(&bars->o_full[t], qn & 1, abort_flag, p, SITE_SOFTMAX_O);
+                ok = __all_sync(0xffffffffu, wt);
+                ++qn;
             }
-            if (store) p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.69314718055994530942f;
+            if (!ok) break;
+            tc_fence_after();
+                float out_mult = 1.0f / l;
+                if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / 256.0f);
+                const bool store = i < p.N;
+                __nv_bfloat16* orow =
+                    reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * p.N + i) * p.H + h) * D;
+    #pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t orr[32];
+                    tmem_ld32(o_tmem + c * 32, orr);
+                    tmem_wait_ld();
+                    reg_fence32(orr);
+                    uint32_t pk[16];
+    #pragma unroll
+                    for (int x = 0; x < 16; ++x)
+                        pk[x] = pack_bf16x2(__uint_as_float(orr[2 * x]) * out_mult,
+                                            __uint_as_float(orr[2 * x + 1]) * out_mult);
+                    if (store) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+    #pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+                    }
+                }
+                if (store) p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.69314718055994530942f;
         }
     }
 

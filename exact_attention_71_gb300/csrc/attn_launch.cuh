@@ -22,7 +22,7 @@ FwdGeometry fwd_geometry() {
 }
 
 template <class Cfg>
-cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t stream) {
+cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int max_ctas, cudaStream_t stream) {
     auto kernel = attn_fwd_kernel<Cfg>;
     // The register split inside the kernel (setmaxnreg) assumes every thread
     // is launched with exactly LAUNCH_REGS registers; a different count could
@@ -35,17 +35,20 @@ cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, cudaStream_t str
     // idempotent, so it is set on every launch (devices may differ per call).
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // Persistent grid: at most one CTA per SM (shared memory allows one), each
+    // walking the items blockIdx.x, blockIdx.x + gridDim.x, ...
     const long long units = static_cast<long long>(p.n_mblocks) * p.B * p.H;
-    kernel<<<dim3(static_cast<unsigned>(units)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream>>>(maps.q, maps.k,
-                                                                                               maps.v, p);
+    const long long grid = units < max_ctas ? units : max_ctas;
+    kernel<<<dim3(static_cast<unsigned>(grid)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream>>>(maps.q, maps.k,
+                                                                                              maps.v, p);
     return cudaGetLastError();
 }
 
 // Per-instantiation entry points (one translation unit each).
-cudaError_t run_fwd_bf16_d64(const FwdMaps&, const FwdParams&, cudaStream_t);
-cudaError_t run_fwd_bf16_d128(const FwdMaps&, const FwdParams&, cudaStream_t);
-cudaError_t run_fwd_bf16_d256(const FwdMaps&, const FwdParams&, cudaStream_t);
-cudaError_t run_fwd_fp8_d128(const FwdMaps&, const FwdParams&, cudaStream_t);
+cudaError_t run_fwd_bf16_d64(const FwdMaps&, const FwdParams&, int, cudaStream_t);
+cudaError_t run_fwd_bf16_d128(const FwdMaps&, const FwdParams&, int, cudaStream_t);
+cudaError_t run_fwd_bf16_d256(const FwdMaps&, const FwdParams&, int, cudaStream_t);
+cudaError_t run_fwd_fp8_d128(const FwdMaps&, const FwdParams&, int, cudaStream_t);
 FwdGeometry geom_bf16_d64();
 FwdGeometry geom_bf16_d128();
 FwdGeometry geom_bf16_d256();

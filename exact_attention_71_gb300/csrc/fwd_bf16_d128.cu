@@ -3,6 +3,8 @@
 
 namespace attn {
 using Cfg_bf16_d128 = FwdCfg<128, 128, 2, false>;
-cudaError_t run_fwd_bf16_d128(const FwdMaps& m, const FwdParams& p, cudaStream_t s) { return launch_fwd<Cfg_bf16_d128>(m, p, s); }
+cudaError_t run_fwd_bf16_d128(const FwdMaps& m, const FwdParams& p, int g, cudaStream_t s) {
+    return launch_fwd<Cfg_bf16_d128>(m, p, g, s);
+}
 FwdGeometry geom_bf16_d128() { return fwd_geometry<Cfg_bf16_d128>(); }
 }  // namespace attn

@@ -3,6 +3,8 @@
 
 namespace attn {
 using Cfg_bf16_d64 = FwdCfg<64, 128, 2, false>;
-cudaError_t run_fwd_bf16_d64(const FwdMaps& m, const FwdParams& p, cudaStream_t s) { return launch_fwd<Cfg_bf16_d64>(m, p, s); }
+cudaError_t run_fwd_bf16_d64(const FwdMaps& m, const FwdParams& p, int g, cudaStream_t s) {
+    return launch_fwd<Cfg_bf16_d64>(m, p, g, s);
+}
 FwdGeometry geom_bf16_d64() { return fwd_geometry<Cfg_bf16_d64>(); }
 }  // namespace attn

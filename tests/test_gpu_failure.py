@@ -30,11 +30,12 @@ def test_wait_timeout_is_reported_and_the_context_survives():
     try:
         api.attn_fwd(qd, kd, vd, causal=True)
         rc, site = api.device_status()
+        msg = lib.attn_last_error_string()
     finally:
         lib.attn_set_wait_limit(0)
     assert rc == ATTN_ERR_DEVICE_TIMEOUT, (rc, site)
     assert site in KNOWN_SITES, hex(site)
-    assert b"gave up" in lib.attn_last_error_string()
+    assert b"gave up" in msg
     # status word cleared, context usable, results correct again
     assert api.device_status()[0] == 0
     o, lse = api.attn_fwd(qd, kd, vd, causal=True)
