@@ -17,7 +17,7 @@ from tests.helpers import assert_bf16_parity, errors, gpu_rows, lse_rows, to_dev
 pytestmark = pytest.mark.gpu
 
 ATTN_ERR_DEVICE_TIMEOUT = -4
-KNOWN_SITES = {0x11, 0x12, 0x21, 0x22, 0x23, 0x24, 0x31, 0x32}
+KNOWN_SITES = {0x11, 0x12, 0x21, 0x22, 0x23, 0x24, 0x31, 0x32, 0x41}
 
 
 def test_wait_timeout_is_reported_and_the_context_survives():
