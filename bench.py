@@ -223,9 +223,9 @@ def cpu_baseline(w, budget_s=12.0, arrs=None):
         t0 = time.perf_counter()
         oracle.attention(q, k, v, causal=w["causal"], window=w["window"], rows=rows, nthreads=cores)
         t = time.perf_counter() - t0
-        if t >= budget_s / 4 or nrows >= N:
+        if t >= budget_s / 2 or nrows >= N:
             break
-        nrows = min(N, int(nrows * max(2.0, min(8.0, (budget_s / 4) / max(t, 1e-3)))))
+        nrows = min(N, int(nrows * max(1.5, min(8.0, 0.6 * budget_s / max(t, 1e-3)))))
     flops = 4.0 * d * pairs_of(rows)
     return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
             "sample": f"{len(rows)} seeded query rows per head x all {B * H} heads of the workload "
@@ -263,7 +263,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c2")
     ap.add_argument("--quick", action="store_true", help="skip e2e, FP8 and CPU baseline (profiling runs)")
-    ap.add_argument("--ref-budget", type=float, default=12.0)
+    ap.add_argument("--ref-budget", type=float, default=20.0)
     args = ap.parse_args()
     w = workload(args.workload)
     if args.impl == "reference":
