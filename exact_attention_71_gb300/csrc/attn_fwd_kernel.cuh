@@ -77,8 +77,11 @@ struct FwdCfg {
     static constexpr int BOX_ELEMS = 128 / ES;
     static constexpr int Q_TILE_BYTES = BM * ROW_BYTES;
     static constexpr int KV_TILE_BYTES = BN * ROW_BYTES;
+    // A ring stage holds what key-tile step u consumes: K_u (for S(u)) and
+    // V_{u-1} (for P(u-1) V), under one barrier.
+    static constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES;
     static constexpr int RING_BUDGET = 196 * 1024 - NQ * Q_TILE_BYTES;
-    static constexpr int NSTAGE_RAW = RING_BUDGET / KV_TILE_BYTES;
+    static constexpr int NSTAGE_RAW = RING_BUDGET / STAGE_BYTES;
     static constexpr int NSTAGE = NSTAGE_RAW > 8 ? 8 : NSTAGE_RAW;
     static constexpr int MMA_K = FP8 ? 32 : 16;          // K per MMA instruction
     static constexpr int P_COLS = BN * ES / 4;           // TMEM columns of one P row
@@ -101,7 +104,7 @@ struct FwdCfg {
     static constexpr int HIGH_REGS_RAW = ((LAUNCH_REGS * THREADS - LOW_REGS * 128) / (NQ * 128)) / 8 * 8;
     static constexpr int HIGH_REGS = HIGH_REGS_RAW > 248 ? 248 : HIGH_REGS_RAW;
     static_assert(HIGH_REGS * NQ * 128 + LOW_REGS * 128 <= LAUNCH_REGS * THREADS, "register split");
-    static constexpr int SMEM_BYTES = 1024 + NQ * Q_TILE_BYTES + NSTAGE * KV_TILE_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + NQ * Q_TILE_BYTES + NSTAGE * STAGE_BYTES + BAR_BYTES;
 
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
     static_assert(BN == 64 || BN == 128, "key tile");
@@ -275,8 +278,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;                                       // NQ x Q tile
-    uint8_t* sKV = smem + NQ * Cfg::Q_TILE_BYTES;             // NSTAGE x KV tile
-    SharedBarriers* bars = reinterpret_cast<SharedBarriers*>(sKV + NSTAGE * Cfg::KV_TILE_BYTES);
+    uint8_t* sKV = smem + NQ * Cfg::Q_TILE_BYTES;             // NSTAGE x (K tile, V tile)
+    SharedBarriers* bars = reinterpret_cast<SharedBarriers*>(sKV + NSTAGE * Cfg::STAGE_BYTES);
     volatile int* abort_flag = &bars->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -345,24 +348,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tma_load_4d(sQ + t * Cfg::Q_TILE_BYTES + cb * (BM * 128), &tmap_q, &bars->q_full[t],
                                     cb * Cfg::BOX_ELEMS, w.h, w.q0 + t * BM, w.b, pol_q);
                 }
-                for (int j = w.u_lo; j <= w.u_hi && ok; ++j) {
-#pragma unroll
-                    for (int kind = 0; kind < 2; ++kind) {
-                        const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
-                        if (!wait_phase(&bars->ring_empty[stage], (round & 1) ^ 1, abort_flag, p,
-                                        SITE_LOAD_EMPTY)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&bars->ring_full[stage], Cfg::KV_TILE_BYTES);
-                        uint8_t* dst = sKV + stage * Cfg::KV_TILE_BYTES;
-                        const CUtensorMap* map = kind == 0 ? &tmap_k : &tmap_v;
+                // Step u in [u_lo, u_hi + 1]: K_u (if u <= u_hi) and V_{u-1} (if u > u_lo).
+                for (int u = w.u_lo; u <= w.u_hi + 1 && ok; ++u) {
+                    const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
+                    if (!wait_phase(&bars->ring_empty[stage], (round & 1) ^ 1, abort_flag, p, SITE_LOAD_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool with_k = u <= w.u_hi, with_v = u > w.u_lo;
+                    mbar_arrive_expect_tx(&bars->ring_full[stage],
+                                          (with_k ? Cfg::KV_TILE_BYTES : 0) + (with_v ? Cfg::KV_TILE_BYTES : 0));
+                    uint8_t* dst = sKV + stage * Cfg::STAGE_BYTES;
+                    if (with_k) {
 #pragma unroll
                         for (int cb = 0; cb < Cfg::NCB; ++cb)
-                            tma_load_4d(dst + cb * (BN * 128), map, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS,
-                                        w.h, j * BN, w.b, pol_kv);
-                        ++it;
+                            tma_load_4d(dst + cb * (BN * 128), &tmap_k, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS,
+                                        w.h, u * BN, w.b, pol_kv);
                     }
+                    if (with_v) {
+#pragma unroll
+                        for (int cb = 0; cb < Cfg::NCB; ++cb)
+                            tma_load_4d(dst + Cfg::KV_TILE_BYTES + cb * (BN * 128), &tmap_v, &bars->ring_full[stage],
+                                        cb * Cfg::BOX_ELEMS, w.h, (u - 1) * BN, w.b, pol_kv);
+                    }
+                    ++it;
                 }
             }
             // Let every copy this warp issued land before the CTA can exit (on
@@ -403,87 +412,55 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ++qn[t];
                 }
             }
-            uint32_t prev_v_stage = 0, prev_v_round = 0;
-            for (int u = w.u_lo; u <= w.u_hi && ok; ++u) {
-                const uint32_t kstage = it % NSTAGE, kround = it / NSTAGE;
+            for (int u = w.u_lo; u <= w.u_hi + 1 && ok; ++u) {
+                const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
                 ++it;
-                const uint32_t vstage = it % NSTAGE, vround = it / NSTAGE;
-                ++it;
-                if (!warp_wait(&bars->ring_full[kstage], kround & 1, abort_flag, p, SITE_MMA_FULL)) {
+                if (!warp_wait(&bars->ring_full[stage], round & 1, abort_flag, p, SITE_MMA_FULL)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t kdesc = sdesc_sw128(sKV_addr + kstage * Cfg::KV_TILE_BYTES, 16, 1024);
-                const uint64_t vdesc_prev = sdesc_sw128(sKV_addr + prev_v_stage * Cfg::KV_TILE_BYTES, BN * 128, 1024);
-                bool v_ready = false;
+                const uint32_t st_addr = sKV_addr + stage * Cfg::STAGE_BYTES;
+                const uint64_t kdesc = sdesc_sw128(st_addr, 16, 1024);
+                const uint64_t vdesc = sdesc_sw128(st_addr + Cfg::KV_TILE_BYTES, BN * 128, 1024);
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
                     if (!w.active[t]) continue;
-                    if (u > w.u_lo && u - 1 >= w.lo[t] && u - 1 <= w.hi[t]) {
-                        if (!v_ready) {
-                            if (!warp_wait(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p,
-                                           SITE_MMA_FULL)) {
-                                ok = false;
-                                break;
-                            }
-                            v_ready = true;
-                        }
+                    const bool do_pv = u > w.u_lo && u - 1 >= w.lo[t] && u - 1 <= w.hi[t];
+                    const bool do_s = u <= w.u_hi && u >= w.lo[t] && u <= w.hi[t];
+                    if (do_pv) {
                         if (!warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
+                    }
+                    if (do_pv || do_s) {
                         if (elect_one()) {
-                            issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev,
-                                          !item_first_pv[t]);
-                            if (u - 1 == w.hi[t]) mma_commit(&bars->o_full[t]);
+                            if (do_pv) {
+                                issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc,
+                                              !item_first_pv[t]);
+                                if (u - 1 == w.hi[t]) mma_commit(&bars->o_full[t]);
+                            }
+                            if (do_s) {
+                                issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
+                                mma_commit(&bars->s_full[t]);
+                                // Q_t is free for the next item once its last S MMA is done.
+                                if (u == w.hi[t]) mma_commit(&bars->q_empty[t]);
+                            }
                         }
                         __syncwarp();
+                    }
+                    if (do_pv) {
                         item_first_pv[t] = false;
                         ++pv_count[t];
                     }
-                    if (u >= w.lo[t] && u <= w.hi[t]) {
-                        if (elect_one()) {
-                            issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
-                            mma_commit(&bars->s_full[t]);
-                            // Q_t is free for the next item once its last S MMA is done.
-                            if (u == w.hi[t]) mma_commit(&bars->q_empty[t]);
-                        }
-                        __syncwarp();
-                    }
                 }
                 if (!ok) break;
-                if (elect_one()) {
-                    mma_commit(&bars->ring_empty[kstage]);
-                    if (u > w.u_lo) mma_commit(&bars->ring_empty[prev_v_stage]);
-                }
+                // The stage is free once this step's MMAs are done.
+                if (elect_one()) mma_commit(&bars->ring_empty[stage]);
                 __syncwarp();
-                prev_v_stage = vstage;
-                prev_v_round = vround;
             }
-            if (!ok) break;
-            // P V of the item's last key tile.
-            ok = warp_wait(&bars->ring_full[prev_v_stage], prev_v_round & 1, abort_flag, p, SITE_MMA_FULL);
-            const uint64_t vdesc_prev = sdesc_sw128(sKV_addr + prev_v_stage * Cfg::KV_TILE_BYTES, BN * 128, 1024);
-#pragma unroll
-            for (int t = 0; t < NQ; ++t) {
-                if (!ok || !w.active[t] || w.u_hi < w.lo[t] || w.u_hi > w.hi[t]) continue;
-                if (!warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
-                    ok = false;
-                    continue;
-                }
-                tc_fence_after();
-                if (elect_one()) {
-                    issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc_prev, !item_first_pv[t]);
-                    mma_commit(&bars->o_full[t]);
-                }
-                __syncwarp();
-                item_first_pv[t] = false;
-                ++pv_count[t];
-            }
-            if (ok && elect_one()) mma_commit(&bars->ring_empty[prev_v_stage]);
-            __syncwarp();
         }
         // Every MMA the elected lane issued has finished before teardown.
         if (elect_one()) {
@@ -602,6 +579,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tmem_st16(s_tmem + c * 16, pk);
                     }
                 } else {
+                    // P * pv_mult = exp2(x + log2(pv_mult)): the V block scale
+                    // rides in the exponent; the tile's sum is divided by it once.
+                    const float lg = __log2f(pv_mult);
+                    const float2 negs = make_float2(-m_use + lg, -m_use + lg);
 #pragma unroll
                     for (int c = 0; c < BN / 64; ++c) {
                         uint32_t pk[16];
@@ -609,19 +590,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         for (int x = 0; x < 16; ++x) {
                             const int e = c * 64 + 4 * x;
                             float2 t0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                                   mult2, neg2);
+                                                   mult2, negs);
                             float2 t1 = __ffma2_rn(
-                                make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), mult2, neg2);
+                                make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), mult2, negs);
                             t0.x = ex2_approx(t0.x);
                             t0.y = ex2_approx(t0.y);
                             t1.x = ex2_approx(t1.x);
                             t1.y = ex2_approx(t1.y);
                             acc0 = __fadd2_rn(acc0, t0);
                             acc1 = __fadd2_rn(acc1, t1);
-                            pk[x] = pack_e4m3x4(t0.x * pv_mult, t0.y * pv_mult, t1.x * pv_mult, t1.y * pv_mult);
+                            pk[x] = pack_e4m3x4(t0.x, t0.y, t1.x, t1.y);
                         }
                         tmem_st16(s_tmem + c * 16, pk);
                     }
+                    const float inv = 1.0f / pv_mult;
+                    acc0.x *= inv; acc0.y *= inv; acc1.x *= inv; acc1.y *= inv;
                 }
                 const float rsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
                 l = l * alpha + rsum;
