@@ -62,6 +62,7 @@ enum : int {
     SITE_MMA_DRAIN = 0x24,
     SITE_SOFTMAX_S = 0x31,
     SITE_SOFTMAX_O = 0x32,
+    SITE_TURN = 0x41,
 };
 
 template <int D_, int BN_, int NQ_, bool FP8_>
@@ -90,7 +91,11 @@ struct FwdCfg {
     static constexpr int TMEM_COLS = 512;
     static constexpr int NUM_SOFTMAX_THREADS = NQ * 128;
     static constexpr int LOAD_WARP = NQ * 4;
-    static constexpr int MMA_WARP = NQ * 4 + 1;
+    static constexpr int MMA_WARP = NQ * 4 + 1;   // MMA warps: MMA_WARP .. MMA_WARP + MMA_WARPS - 1
+    // Issuer warps: one per query tile where the tile's MMAs are long enough
+    // (bf16, d = 128) for the hand-off latency to dominate; one warp for both
+    // tiles where the softmax is the longer phase (FP8, d = 64) or NQ = 1.
+    static constexpr int MMA_WARPS = (!FP8 && D == 128 && NQ == 2) ? 2 : 1;
     static constexpr int THREADS = NQ * 128 + 128;
     static constexpr int BAR_BYTES = 256;
     // The reference maximum of a row moves only when the row maximum exceeds
@@ -120,11 +125,12 @@ struct SharedBarriers {
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_full[2];
-    uint64_t drain;
+    uint64_t drain[2];
     uint64_t ring_full[8];
     uint64_t ring_empty[8];
     uint32_t tmem_base;
     int abort_flag;
+    int issued_blocks;    // MMA blocks issued so far (ping-pong turn counter)
 };
 
 // Bounded wait on an mbarrier phase.  Returns false when the shared abort
@@ -232,6 +238,48 @@ __device__ __forceinline__ WorkItem<Cfg::NQ> decode_item(const FwdParams& p, int
     return w;
 }
 
+// MMA issue order of an item (the ping-pong of the two query tiles): for
+// u = u_lo .. u_hi + 1 and t = 0, 1 the block (t, u) holds O_t += P_t V_{u-1}
+// (when key tile u-1 is in tile t's range) and S_t = Q_t K_u^T (when u is);
+// empty blocks are skipped.  Returns the number of blocks before (t, u).
+template <int NQ>
+__device__ __forceinline__ int blocks_before(const WorkItem<NQ>& w, int t, int u) {
+    int n = 0;
+#pragma unroll
+    for (int x = 0; x < NQ; ++x)
+        if (w.active[x]) n += min(max(u - w.lo[x], 0), w.hi[x] - w.lo[x] + 2);
+    if (NQ > 1 && t == 1 && w.active[0] && u >= w.lo[0] && u <= w.hi[0] + 1) ++n;
+    return n;
+}
+
+template <int NQ>
+__device__ __forceinline__ int item_blocks(const WorkItem<NQ>& w) {
+    int n = 0;
+#pragma unroll
+    for (int x = 0; x < NQ; ++x)
+        if (w.active[x]) n += w.hi[x] - w.lo[x] + 2;
+    return n;
+}
+
+// Bounded wait (whole warp) until `k` MMA blocks have been issued.
+__device__ __forceinline__ bool wait_turn(volatile int* issued, int k, volatile int* abort_flag,
+                                          const FwdParams& p, int site) {
+    bool ok = true;
+    if (*issued < k) {
+        const long long t0 = clock64();
+        while (*issued < k) {
+            if (*abort_flag) { ok = false; break; }
+            if (static_cast<unsigned long long>(clock64() - t0) > p.wait_limit) {
+                *abort_flag = 1;
+                atomicCAS(p.status, 0, site);
+                ok = false;
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
 // S_t = Q_t K^T: D / MMA_K instructions, operands in shared memory (both
 // K-major, 128-byte swizzle); each k-step advances the descriptors' start
 // address by a constant.
@@ -293,12 +341,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             mbar_init(&bars->p_full[t], 128);
             mbar_init(&bars->o_full[t], 1);
         }
-        mbar_init(&bars->drain, 1);
+        mbar_init(&bars->drain[0], 1);
+        mbar_init(&bars->drain[1], 1);
         for (int s = 0; s < 8; ++s) {
             mbar_init(&bars->ring_full[s], 1);
-            mbar_init(&bars->ring_empty[s], 1);
+            mbar_init(&bars->ring_empty[s], Cfg::MMA_WARPS);
         }
         bars->abort_flag = 0;
+        bars->issued_blocks = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -384,30 +434,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (qn[t] > 0) drain_wait(&bars->q_full[t], (qn[t] - 1) & 1, p, SITE_LOAD_DRAIN);
         }
         __syncwarp();
-    } else if (warp == Cfg::MMA_WARP) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs the loop (waits, descriptor arithmetic) so the
-        // descriptors stay warp-uniform; one elected lane issues the MMAs and
-        // their commits (a commit tracks the MMAs of the issuing thread).
-        const uint32_t sQ_addr = smem_u32(sQ);
+    } else if (warp >= Cfg::MMA_WARP && warp < Cfg::MMA_WARP + Cfg::MMA_WARPS) {
+        // ------------------------------------------------------------ MMA issuers
+        // Issuer warp w owns the query tiles t = w, w + MMA_WARPS, ...  Issuing
+        // one tcgen05.mma takes tens of cycles, so with long MMAs one warp cannot
+        // feed two tiles and also answer their P hand-offs in time; with a warp
+        // per tile, one waits for its P while the other issues.  The blocks go
+        // to the tensor pipe in the ping-pong order either way (a turn counter
+        // in shared memory when there are two issuers), so the two softmax
+        // warpgroups stay out of phase.  The whole warp runs the loop
+        // (descriptors stay warp-uniform); one elected lane issues the MMAs and
+        // the commits.  Each issuer releases every ring stage once (ring_empty
+        // counts MMA_WARPS), always after waiting for its load, so no issuer can
+        // get a ring cycle ahead.
+        constexpr int MW = Cfg::MMA_WARPS;
+        const int wi = warp - Cfg::MMA_WARP;
         const uint32_t sKV_addr = smem_u32(sKV);
+        volatile int* issued = &bars->issued_blocks;
         uint64_t qdesc[NQ];
 #pragma unroll
-        for (int t = 0; t < NQ; ++t) qdesc[t] = sdesc_sw128(sQ_addr + t * Cfg::Q_TILE_BYTES, 16, 1024);
+        for (int t = 0; t < NQ; ++t) qdesc[t] = sdesc_sw128(smem_u32(sQ) + t * Cfg::Q_TILE_BYTES, 16, 1024);
         uint32_t it = 0;
         uint32_t pv_count[NQ], qn[NQ];
 #pragma unroll
         for (int t = 0; t < NQ; ++t) pv_count[t] = qn[t] = 0;
+        int item_base = 0;
         bool ok = true;
         for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
             const int item = round_item(rnd);
             if (item >= total_items) continue;
             const WorkItem<NQ> w = decode_item<Cfg>(p, item);
-            bool item_first_pv[NQ];
+            bool first_pv[NQ];
 #pragma unroll
             for (int t = 0; t < NQ; ++t) {
-                item_first_pv[t] = true;
-                if (w.active[t] && ok) {
+                first_pv[t] = true;
+                if (t % MW == wi && w.active[t] && ok) {
                     ok = warp_wait(&bars->q_full[t], qn[t] & 1, abort_flag, p, SITE_MMA_Q);
                     ++qn[t];
                 }
@@ -419,53 +480,63 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 const uint32_t st_addr = sKV_addr + stage * Cfg::STAGE_BYTES;
                 const uint64_t kdesc = sdesc_sw128(st_addr, 16, 1024);
                 const uint64_t vdesc = sdesc_sw128(st_addr + Cfg::KV_TILE_BYTES, BN * 128, 1024);
+                bool issued_any = false;
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
-                    if (!w.active[t]) continue;
-                    const bool do_pv = u > w.u_lo && u - 1 >= w.lo[t] && u - 1 <= w.hi[t];
-                    const bool do_s = u <= w.u_hi && u >= w.lo[t] && u <= w.hi[t];
-                    if (do_pv) {
-                        if (!warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+                    if (t % MW != wi || !w.active[t]) continue;
+                    const bool do_pv = u - 1 >= w.lo[t] && u - 1 <= w.hi[t];
+                    const bool do_s = u <= w.hi[t] && u >= w.lo[t];
+                    if (!do_pv && !do_s) continue;
+                    if (do_pv && !warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
+                        ok = false;
+                        break;
                     }
-                    if (do_pv || do_s) {
-                        if (elect_one()) {
-                            if (do_pv) {
-                                issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc,
-                                              !item_first_pv[t]);
-                                if (u - 1 == w.hi[t]) mma_commit(&bars->o_full[t]);
-                            }
-                            if (do_s) {
-                                issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
-                                mma_commit(&bars->s_full[t]);
-                                // Q_t is free for the next item once its last S MMA is done.
-                                if (u == w.hi[t]) mma_commit(&bars->q_empty[t]);
-                            }
-                        }
-                        __syncwarp();
+                    const int k = item_base + blocks_before(w, t, u);
+                    if (MW > 1 && !wait_turn(issued, k, abort_flag, p, SITE_TURN)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    if (elect_one()) {
+                        if (do_pv) {
+                            issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc, !first_pv[t]);
+                            if (u - 1 == w.hi[t]) mma_commit(&bars->o_full[t]);
+                        }
+                        if (do_s) {
+                            issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
+                            mma_commit(&bars->s_full[t]);
+                            // Q_t is free for the next item once its last S MMA is done.
+                            if (u == w.hi[t]) mma_commit(&bars->q_empty[t]);
+                        }
+                        if (MW > 1) {
+                            __threadfence_block();
+                            *issued = k + 1;
+                        }
+                    }
+                    __syncwarp();
+                    issued_any = true;
                     if (do_pv) {
-                        item_first_pv[t] = false;
+                        first_pv[t] = false;
                         ++pv_count[t];
                     }
                 }
                 if (!ok) break;
-                // The stage is free once this step's MMAs are done.
-                if (elect_one()) mma_commit(&bars->ring_empty[stage]);
+                // This issuer is done with the stage once its MMAs of the step are.
+                if (elect_one()) {
+                    if (issued_any) mma_commit(&bars->ring_empty[stage]);
+                    else mbar_arrive(&bars->ring_empty[stage]);
+                }
                 __syncwarp();
             }
+            item_base += item_blocks(w);
         }
-        // Every MMA the elected lane issued has finished before teardown.
+        // Every MMA this warp issued has finished before teardown.
         if (elect_one()) {
-            mma_commit(&bars->drain);
-            drain_wait(&bars->drain, 0, p, SITE_MMA_DRAIN);
+            mma_commit(&bars->drain[wi]);
+            drain_wait(&bars->drain[wi], 0, p, SITE_MMA_DRAIN);
         }
         __syncwarp();
     }
