@@ -35,66 +35,74 @@ __device__ __forceinline__ float diag_sign(unsigned long long seed, int c) {
 
 enum Pass { kFused = 0, kAmaxOnly = 1, kApplyScale = 2 };
 
+// x / s rounded to nearest for s > 0, from the correctly rounded reciprocal
+// and one residual correction (Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. R&D 1990): with
+// inv = RN(1/s), q0 = RN(x * inv) and the exact residual x - q0 * s (one FMA),
+// q0 + residual * inv rounds to RN(x / s) for the normal-range quotients
+// here (|x / s| <= 448).  The sign is copied so that -0 / s stays -0.
+__device__ __forceinline__ float div_by_scale(float x, float s, float inv) {
+    const float q0 = x * inv;
+    const float rem = fmaf(-q0, s, x);
+    return copysignf(fmaf(rem, inv, q0), x);
+}
+
+template <int E> struct RowLoad;
+template <> struct RowLoad<2> { using T = uint32_t; };
+template <> struct RowLoad<4> { using T = uint2; };
+template <> struct RowLoad<8> { using T = uint4; };
+
 template <int D, int WARPS, int PASS>
 __global__ void __launch_bounds__(WARPS * 32)
     fp8_prep_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ x8, float* __restrict__ scales,
                     int H, int N, int nblk, int rotate, unsigned long long seed) {
     constexpr int E = D / 32;                     // elements per lane
     constexpr int RPW = kBlockRows / WARPS;       // rows per warp
+    using Raw = typename RowLoad<E>::T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int blk = blockIdx.x % nblk;
     const int bh = blockIdx.x / nblk;
     const int b = bh / H, h = bh % H;
-    const int n0 = blk * kBlockRows;
+    const int n0 = blk * kBlockRows + warp * RPW;
 
-    float r[RPW][E];
+    // Issue every row load of this thread before any arithmetic.
+    Raw raw[RPW];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int n = n0 + rr;
+        if (n < N) {
+            raw[rr] = __ldg(reinterpret_cast<const Raw*>(x + ((static_cast<size_t>(b) * N + n) * H + h) * D + lane * E));
+        } else {
+            raw[rr] = Raw{};
+        }
+    }
+
     float sgn[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) sgn[e] = rotate ? diag_sign(seed, lane * E + e) : 1.0f;
 
+    float r[RPW][E];
     float amax = 0.0f;
 #pragma unroll
     for (int rr = 0; rr < RPW; ++rr) {
-        const int n = n0 + warp * RPW + rr;
-        if (n < N) {
-            const __nv_bfloat16* src = x + ((static_cast<size_t>(b) * N + n) * H + h) * D + lane * E;
-            if constexpr (E == 2) {
-                const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(src);
-                r[rr][0] = __bfloat162float(v.x);
-                r[rr][1] = __bfloat162float(v.y);
-            } else if constexpr (E == 4) {
-                const uint2 v = *reinterpret_cast<const uint2*>(src);
-                const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&v);
+        const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&raw[rr]);
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    r[rr][2 * k] = __bfloat162float(pv[k].x);
-                    r[rr][2 * k + 1] = __bfloat162float(pv[k].y);
-                }
-            } else {
-                const uint4 v = *reinterpret_cast<const uint4*>(src);
-                const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    r[rr][2 * k] = __bfloat162float(pv[k].x);
-                    r[rr][2 * k + 1] = __bfloat162float(pv[k].y);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < E; ++e) r[rr][e] = 0.0f;
+        for (int k = 0; k < E / 2; ++k) {
+            r[rr][2 * k] = __bfloat162float(pv[k].x);
+            r[rr][2 * k + 1] = __bfloat162float(pv[k].y);
         }
         if (rotate) {
 #pragma unroll
             for (int e = 0; e < E; ++e) r[rr][e] *= sgn[e];
             // Butterflies inside the thread (strides 1 .. E/2).
 #pragma unroll
-            for (int s = 1; s < E; s <<= 1) {
+            for (int st = 1; st < E; st <<= 1) {
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
-                    if ((e & s) == 0) {
-                        const float a = r[rr][e], c = r[rr][e + s];
+                    if ((e & st) == 0) {
+                        const float a = r[rr][e], c = r[rr][e + st];
                         r[rr][e] = a + c;
-                        r[rr][e + s] = a - c;
+                        r[rr][e + st] = a - c;
                     }
                 }
             }
@@ -132,9 +140,9 @@ __global__ void __launch_bounds__(WARPS * 32)
             if constexpr (PASS == kAmaxOnly) {
                 scales[static_cast<size_t>(bh) * nblk + blk] = a;
             } else {
-                const float s = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
-                scales[static_cast<size_t>(bh) * nblk + blk] = s;
-                block_scale = s;
+                const float sc = a > 0.0f ? __fdiv_rn(a, 448.0f) : 1.0f;
+                scales[static_cast<size_t>(bh) * nblk + blk] = sc;
+                block_scale = sc;
             }
         }
         if constexpr (PASS == kAmaxOnly) return;
@@ -143,27 +151,26 @@ __global__ void __launch_bounds__(WARPS * 32)
         if (threadIdx.x == 0) block_scale = scales[static_cast<size_t>(bh) * nblk + blk];
         __syncthreads();
     }
-    const float s = block_scale;
+    const float sc = block_scale;
+    const float inv = __frcp_rn(sc);
 #pragma unroll
     for (int rr = 0; rr < RPW; ++rr) {
-        const int n = n0 + warp * RPW + rr;
+        const int n = n0 + rr;
         if (n >= N) continue;
         uint8_t* dst = x8 + ((static_cast<size_t>(b) * N + n) * H + h) * D + lane * E;
+        float y[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) y[e] = div_by_scale(r[rr][e], sc, inv);
         if constexpr (E == 2) {
             uint16_t v;
-            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-                : "=h"(v)
-                : "f"(__fdiv_rn(r[rr][1], s)), "f"(__fdiv_rn(r[rr][0], s)));
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(v) : "f"(y[1]), "f"(y[0]));
             *reinterpret_cast<uint16_t*>(dst) = v;
         } else if constexpr (E == 4) {
-            *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(__fdiv_rn(r[rr][0], s), __fdiv_rn(r[rr][1], s),
-                                                            __fdiv_rn(r[rr][2], s), __fdiv_rn(r[rr][3], s));
+            *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(y[0], y[1], y[2], y[3]);
         } else {
             uint2 v;
-            v.x = pack_e4m3x4(__fdiv_rn(r[rr][0], s), __fdiv_rn(r[rr][1], s), __fdiv_rn(r[rr][2], s),
-                              __fdiv_rn(r[rr][3], s));
-            v.y = pack_e4m3x4(__fdiv_rn(r[rr][4], s), __fdiv_rn(r[rr][5], s), __fdiv_rn(r[rr][6], s),
-                              __fdiv_rn(r[rr][7], s));
+            v.x = pack_e4m3x4(y[0], y[1], y[2], y[3]);
+            v.y = pack_e4m3x4(y[4], y[5], y[6], y[7]);
             *reinterpret_cast<uint2*>(dst) = v;
         }
     }
@@ -214,9 +221,9 @@ cudaError_t launch_prep(const void* x, void* x8, float* scales, int B, int H, in
 cudaError_t run_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, int d, int mode,
                          unsigned long long sign_seed, bool is_v, cudaStream_t stream) {
     switch (d) {
-        case 64: return launch_prep<64, 8>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
-        case 128: return launch_prep<128, 8>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
-        case 256: return launch_prep<256, 16>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
+        case 64: return launch_prep<64, 16>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
+        case 128: return launch_prep<128, 16>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
+        case 256: return launch_prep<256, 32>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
         default: return cudaErrorInvalidValue;
     }
 }
