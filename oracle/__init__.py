@@ -40,9 +40,9 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(_LIB)
             P = ctypes.c_void_p
             i, d, u64, lng = ctypes.c_int, ctypes.c_double, ctypes.c_ulonglong, ctypes.c_long
-            L.oracle_attn_fwd_bf16.argtypes = [P, P, P, P, P, i, i, i, i, i, d, i, P, i, i]
+            L.oracle_attn_fwd_bf16.argtypes = [P, P, P, P, P, i, i, i, i, i, i, d, i, P, i, i]
             L.oracle_attn_fwd_bf16.restype = i
-            L.oracle_attn_fwd_f64.argtypes = [P, P, P, P, P, i, i, i, i, i, d, i, P, i, i]
+            L.oracle_attn_fwd_f64.argtypes = [P, P, P, P, P, i, i, i, i, i, i, d, i, P, i, i]
             L.oracle_attn_fwd_f64.restype = i
             L.oracle_attn_row_probs_f64.argtypes = [P, P, P, i, i, i, i, i, d, i, i, i, i, P]
             L.oracle_attn_row_probs_f64.restype = i
@@ -74,11 +74,14 @@ def _rows_arg(rows, N):
 def attention(q, k, v, causal=False, scale=None, window=0, rows=None, nthreads=0):
     """Attention forward in fp64.
 
-    q, k, v: (B, N, H, d) arrays, either uint16 bf16 bit patterns or float64.
-    Returns (o, lse) with o of shape (B, H, R, d) and lse (B, H, R), where R
-    indexes ``rows`` (all N rows when None).
+    q: (B, N, H, d); k, v: (B, N, Hkv, d) with Hkv dividing H (grouped-query
+    attention: query head h reads key/value head h // (H // Hkv)).  Arrays are
+    either uint16 bf16 bit patterns or float64.  Returns (o, lse) with o of
+    shape (B, H, R, d) and lse (B, H, R), where R indexes ``rows`` (all N rows
+    when None).
     """
     B, N, H, d = q.shape
+    Hkv = k.shape[2]
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     rr, R, rp = _rows_arg(rows, N)
@@ -90,7 +93,7 @@ def attention(q, k, v, causal=False, scale=None, window=0, rows=None, nthreads=0
     else:
         fn = lib().oracle_attn_fwd_f64
         q, k, v = (np.ascontiguousarray(t, dtype=np.float64) for t in (q, k, v))
-    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d, int(bool(causal)),
             float(scale), int(window), rp, R, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_attn_fwd: bad arguments")

@@ -138,13 +138,18 @@ void attention_row(const In& qin, const In& kin, const In& vin, long b, long h, 
     }
 }
 
+// A (B, N, heads, d) tensor read by query head h: with grouped-query
+// attention (deep-reading report §3.4) query head h reads key/value head
+// h / group, where group = query heads / key-value heads.
 struct Bf16Tensor {
-    const uint16_t* p; long N, H, d;
-    double operator()(long b, long n, long h, long c) const { return bf16_value(p[((b * N + n) * H + h) * d + c]); }
+    const uint16_t* p; long N, H, d, group;
+    double operator()(long b, long n, long h, long c) const {
+        return bf16_value(p[((b * N + n) * H + h / group) * d + c]);
+    }
 };
 struct F64Tensor {
-    const double* p; long N, H, d;
-    double operator()(long b, long n, long h, long c) const { return p[((b * N + n) * H + h) * d + c]; }
+    const double* p; long N, H, d, group;
+    double operator()(long b, long n, long h, long c) const { return p[((b * N + n) * H + h / group) * d + c]; }
 };
 
 // Output layout: o is (B, H, R, d) and lse is (B, H, R), R = number of rows
@@ -241,19 +246,22 @@ bool is_pow2(long d) { return d > 0 && (d & (d - 1)) == 0; }
 
 extern "C" {
 
+// Q has H heads, K and V have Hkv heads (Hkv divides H).
 int oracle_attn_fwd_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                         double* o, double* lse, int B, int H, int N, int d,
+                         double* o, double* lse, int B, int H, int Hkv, int N, int d,
                          int causal, double scale, int window,
                          const int* rows, int nrows, int nthreads) {
-    Bf16Tensor Q{q, N, H, d}, K{k, N, H, d}, V{v, N, H, d};
+    if (Hkv <= 0 || H % Hkv != 0) return -1;
+    Bf16Tensor Q{q, N, H, d, 1}, K{k, N, Hkv, d, H / Hkv}, V{v, N, Hkv, d, H / Hkv};
     return run_attention(Q, K, V, o, lse, B, H, N, d, causal, scale, window, rows, nrows, nthreads);
 }
 
 int oracle_attn_fwd_f64(const double* q, const double* k, const double* v,
-                        double* o, double* lse, int B, int H, int N, int d,
+                        double* o, double* lse, int B, int H, int Hkv, int N, int d,
                         int causal, double scale, int window,
                         const int* rows, int nrows, int nthreads) {
-    F64Tensor Q{q, N, H, d}, K{k, N, H, d}, V{v, N, H, d};
+    if (Hkv <= 0 || H % Hkv != 0) return -1;
+    F64Tensor Q{q, N, H, d, 1}, K{k, N, Hkv, d, H / Hkv}, V{v, N, Hkv, d, H / Hkv};
     return run_attention(Q, K, V, o, lse, B, H, N, d, causal, scale, window, rows, nrows, nthreads);
 }
 
@@ -262,7 +270,7 @@ int oracle_attn_row_probs_f64(const double* q, const double* k, const double* v,
                               int B, int H, int N, int d, int causal, double scale, int window,
                               int b, int h, int i, double* probs) {
     if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= N) return -1;
-    F64Tensor Q{q, N, H, d}, K{k, N, H, d}, V{v, N, H, d};
+    F64Tensor Q{q, N, H, d, 1}, K{k, N, H, d, 1}, V{v, N, H, d, 1};
     std::vector<double> orow(d);
     double lse;
     attention_row(Q, K, V, b, h, i, N, d, causal, scale, window, orow.data(), &lse, probs);

@@ -153,3 +153,27 @@ def test_bad_rows_rejected():
     q, k, v = synth.qkv_bf16(1, 10, 1, 8, seed=2)
     with pytest.raises(ValueError):
         oracle.attention(q, k, v, rows=[0, 10])
+
+
+@pytest.mark.parametrize("Hkv", [1, 2, 3])
+def test_grouped_query_heads_equal_repeated_key_value_heads(Hkv):
+    """GQA/MQA (deep-reading report §3.4): query head h reads key/value head
+    h // group; pinned against the plain multi-head oracle on K and V whose
+    heads are repeated group times with numpy."""
+    B, N, H, d = 2, 21, 6, 8
+    rng = np.random.default_rng(Hkv)
+    q = rng.standard_normal((B, N, H, d))
+    k = rng.standard_normal((B, N, Hkv, d))
+    v = rng.standard_normal((B, N, Hkv, d))
+    o, lse = oracle.attention(q, k, v, causal=True, window=5)
+    group = H // Hkv
+    o_ref, lse_ref = oracle.attention(q, np.repeat(k, group, axis=2), np.repeat(v, group, axis=2),
+                                      causal=True, window=5)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(lse, lse_ref)
+
+
+def test_grouped_heads_must_divide():
+    q = np.zeros((1, 4, 6, 8)); k = np.zeros((1, 4, 4, 8))
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, k)
