@@ -43,6 +43,8 @@ WORKLOADS = {
                B=2, H=16, N=8192, d=128, causal=False, window=0, dtype="fp8"),
     "c5": dict(name="bf16 fwd B=1 H=8 N=32768 d=128 causal, 4096-token sliding window", B=1, H=8, N=32768,
                d=128, causal=True, window=4096, dtype="bf16"),
+    "gqa": dict(name="bf16 fwd grouped-query B=2 H=32 H_kv=8 N=8192 d=128 causal", B=2, H=32, Hkv=8, N=8192,
+                d=128, causal=True, window=0, dtype="bf16"),
 }
 
 
@@ -181,7 +183,11 @@ def make_inputs(w, device, seed=0):
 
     from exact_attention_71_gb300 import synth
     outliers = w["dtype"] == "fp8"
-    arrs = synth.qkv_bf16(w["B"], w["N"], w["H"], w["d"], seed=seed, outliers=outliers)
+    B, N, H, d = w["B"], w["N"], w["H"], w["d"]
+    Hkv = w.get("Hkv", H)
+    arrs = (synth.tensor_bf16((B, N, H, d), seed, synth.STREAM_Q, outliers),
+            synth.tensor_bf16((B, N, Hkv, d), seed, synth.STREAM_K, outliers),
+            synth.tensor_bf16((B, N, Hkv, d), seed, synth.STREAM_V, outliers))
     return [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device) for a in arrs], arrs
 
 
@@ -206,7 +212,11 @@ def cpu_baseline(w, budget_s=12.0, arrs=None):
     from exact_attention_71_gb300 import synth
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     if arrs is None:
-        arrs = synth.qkv_bf16(B, N, H, d, seed=0, outliers=w["dtype"] == "fp8")
+        Hkv = w.get("Hkv", H)
+        o_ = w["dtype"] == "fp8"
+        arrs = (synth.tensor_bf16((B, N, H, d), 0, synth.STREAM_Q, o_),
+                synth.tensor_bf16((B, N, Hkv, d), 0, synth.STREAM_K, o_),
+                synth.tensor_bf16((B, N, Hkv, d), 0, synth.STREAM_V, o_))
     q, k, v = arrs
     cores = os.cpu_count() or 1
 
@@ -361,7 +371,8 @@ def main():
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w["dtype"] == "bf16" else "e4m3", "data": "synthetic",
-            "config": {"workload": w["name"], "B": B, "H": H, "N": N, "d": d, "causal": w["causal"],
+            "config": {"workload": w["name"], "B": B, "H": H, "H_kv": w.get("Hkv", H), "N": N, "d": d,
+                       "causal": w["causal"],
                        "window": w["window"], "flops_per_step": flops,
                        "flop_convention": "4 B H N^2 d, halved for causal; window: 4 d x attended pairs",
                        "l2": "inputs larger than L2 (two resident input sets, alternated per step)",

@@ -47,6 +47,10 @@ def library() -> ctypes.CDLL:
         L.attn_fwd.restype = i
         L.attn_fwd_fp8.argtypes = [P, P, P, P, P, i, i, i, i, i, f, i, P, P, P, P]
         L.attn_fwd_fp8.restype = i
+        L.attn_fwd_gqa.argtypes = [P, P, P, P, P, i, i, i, i, i, i, f, i, P]
+        L.attn_fwd_gqa.restype = i
+        L.attn_fwd_fp8_gqa.argtypes = [P, P, P, P, P, i, i, i, i, i, i, f, i, P, P, P, P]
+        L.attn_fwd_fp8_gqa.restype = i
         L.attn_fp8_prep.argtypes = [P, P, P, i, i, i, i, i, i, u64, i, P]
         L.attn_fp8_prep.restype = i
         L.attn_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
@@ -80,8 +84,11 @@ def _ptr(t):
 def _check_qkv(q, k, v, dtype):
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k, v must be CUDA tensors")
-    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
-        raise ValueError("q, k, v must share one (batch, seqlen, heads, head_dim) shape")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be (B, N, H, d) and k, v one (B, N, H_kv, d) shape")
+    B, N, H, d = q.shape
+    if k.shape[0] != B or k.shape[1] != N or k.shape[3] != d or H % k.shape[2] != 0:
+        raise ValueError("k, v must be (B, N, H_kv, d) with H_kv dividing the query heads")
     for t in (q, k, v):
         if t.dtype != dtype:
             raise ValueError(f"expected dtype {dtype}, got {t.dtype}")
@@ -104,16 +111,24 @@ def _outputs(q, out, lse):
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0,
              out=None, lse=None, stream=None):
-    """bf16 fused attention forward.  q, k, v: (B, N, H, d) bf16 CUDA tensors.
+    """bf16 fused attention forward.  q: (B, N, H, d); k, v: (B, N, H_kv, d)
+    bf16 CUDA tensors, H_kv dividing H (H_kv < H: grouped-query attention).
 
     Returns (O (B, N, H, d) bf16, LSE (B, H, N) float32, natural log).
     """
     _check_qkv(q, k, v, torch.bfloat16)
     out, lse = _outputs(q, out, lse)
     B, N, H, d = q.shape
-    rc = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
-                            float(scale or 0.0), int(window), ctypes.c_void_p(_stream(stream)))
-    _check("attn_fwd", rc)
+    Hkv = k.shape[2]
+    if Hkv == H:
+        rc = library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d, int(bool(causal)),
+                                float(scale or 0.0), int(window), ctypes.c_void_p(_stream(stream)))
+        _check("attn_fwd", rc)
+    else:
+        rc = library().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                                    int(bool(causal)), float(scale or 0.0), int(window),
+                                    ctypes.c_void_p(_stream(stream)))
+        _check("attn_fwd_gqa", rc)
     return out, lse
 
 
@@ -148,18 +163,21 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, sc
     for t in (q8, k8, v8):
         if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or not t.is_cuda or not t.is_contiguous():
             raise ValueError("q8, k8, v8 must be contiguous e4m3 codes on the GPU")
-    if q8.dim() != 4 or q8.shape != k8.shape or q8.shape != v8.shape:
-        raise ValueError("q8, k8, v8 must share one (B, N, H, d) shape")
+    if q8.dim() != 4 or k8.dim() != 4 or k8.shape != v8.shape:
+        raise ValueError("q8 must be (B, N, H, d) and k8, v8 one (B, N, H_kv, d) shape")
     B, N, H, d = q8.shape
+    Hkv = k8.shape[2]
+    if k8.shape[0] != B or k8.shape[1] != N or k8.shape[3] != d or H % Hkv != 0:
+        raise ValueError("k8, v8 must be (B, N, H_kv, d) with H_kv dividing the query heads")
     nblk = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
-    for s in (q_scale, k_scale, v_scale):
-        if s.shape != (B, H, nblk) or s.dtype != torch.float32 or not s.is_contiguous():
-            raise ValueError("scales must be contiguous float32 (B, H, ceil(N/128)) tensors")
+    for s, heads in ((q_scale, H), (k_scale, Hkv), (v_scale, Hkv)):
+        if s.shape != (B, heads, nblk) or s.dtype != torch.float32 or not s.is_contiguous():
+            raise ValueError("scales must be contiguous float32 (B, heads, ceil(N/128)) tensors")
     out, lse = _outputs(q8, out, lse)
-    rc = library().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(out), _ptr(lse), B, H, N, d,
-                                int(bool(causal)), float(scale or 0.0), int(window), _ptr(q_scale),
-                                _ptr(k_scale), _ptr(v_scale), ctypes.c_void_p(_stream(stream)))
-    _check("attn_fwd_fp8", rc)
+    rc = library().attn_fwd_fp8_gqa(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                                    int(bool(causal)), float(scale or 0.0), int(window), _ptr(q_scale),
+                                    _ptr(k_scale), _ptr(v_scale), ctypes.c_void_p(_stream(stream)))
+    _check("attn_fwd_fp8_gqa", rc)
     return out, lse
 
 

@@ -134,8 +134,8 @@ float resolve_scale(float scale, int d) {
     return scale;
 }
 
-int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                   int d, int causal, float scale, int window, const float* qs, const float* ks, const float* vs,
+int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                   int N, int d, int causal, float scale, int window, const float* qs, const float* ks, const float* vs,
                    void* stream) {
     attn::FwdGeometry g;
     cudaError_t (*run)(const attn::FwdMaps&, const attn::FwdParams&, int, cudaStream_t) = nullptr;
@@ -156,8 +156,8 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
     attn::FwdMaps maps;
     int rc;
     if ((rc = make_map(&maps.q, q, B, H, N, d, g.elem_bytes, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(&maps.k, k, B, H, N, d, g.elem_bytes, g.bn)) != ATTN_OK) return rc;
-    if ((rc = make_map(&maps.v, v, B, H, N, d, g.elem_bytes, g.bn)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.k, k, B, Hkv, N, d, g.elem_bytes, g.bn)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.v, v, B, Hkv, N, d, g.elem_bytes, g.bn)) != ATTN_OK) return rc;
     attn::FwdParams p{};
     p.o = o;
     p.lse = lse;
@@ -167,6 +167,7 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
     p.B = B;
     p.H = H;
     p.N = N;
+    p.group = H / Hkv;
     p.causal = causal ? 1 : 0;
     p.window = window;
     p.scale_log2 = resolve_scale(scale, d) * 1.4426950408889634f;
@@ -186,23 +187,41 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
              int causal, float scale, int window, void* stream) {
+    return attn_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, window, stream);
+}
+
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                 int d, int causal, float scale, int window, void* stream) {
     g_err[0] = '\0';
     int rc = check_common(q, k, v, o, lse, B, H, N, d, window);
-    if (rc != ATTN_OK || static_cast<long long>(B) * H * N == 0) return rc;
-    return launch_forward(false, q, k, v, o, lse, B, H, N, d, causal, scale, window, nullptr, nullptr, nullptr,
-                          stream);
+    if (rc != ATTN_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    return launch_forward(false, q, k, v, o, lse, B, H, H_kv, N, d, causal, scale, window, nullptr, nullptr,
+                          nullptr, stream);
 }
 
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse, int B, int H, int N, int d,
                  int causal, float scale, int window, const float* q_scale, const float* k_scale,
                  const float* v_scale, void* stream) {
+    return attn_fwd_fp8_gqa(q8, k8, v8, o, lse, B, H, H, N, d, causal, scale, window, q_scale, k_scale, v_scale,
+                            stream);
+}
+
+int attn_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o, float* lse, int B, int H, int H_kv,
+                     int N, int d, int causal, float scale, int window, const float* q_scale, const float* k_scale,
+                     const float* v_scale, void* stream) {
     g_err[0] = '\0';
     int rc = check_common(q8, k8, v8, o, lse, B, H, N, d, window);
-    if (rc != ATTN_OK || static_cast<long long>(B) * H * N == 0) return rc;
+    if (rc != ATTN_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
     if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 only (got %d)", d);
     if (!q_scale || !k_scale || !v_scale) return fail(ATTN_ERR_INVALID_ARG, "null scale pointer");
-    return launch_forward(true, q8, k8, v8, o, lse, B, H, N, d, causal, scale, window, q_scale, k_scale, v_scale,
-                          stream);
+    return launch_forward(true, q8, k8, v8, o, lse, B, H, H_kv, N, d, causal, scale, window, q_scale, k_scale,
+                          v_scale, stream);
 }
 
 int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, int d, int block_rows, int mode,

@@ -45,6 +45,7 @@ struct FwdParams {
     const float* k_scale;
     const float* v_scale;
     int B, H, N;
+    int group;               // query heads per key/value head (1 = multi-head)
     int causal, window;
     float scale_log2;        // softmax scale * log2(e)
     int n_mblocks;           // ceil(N / (NQ * 128))
@@ -413,13 +414,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                         for (int cb = 0; cb < Cfg::NCB; ++cb)
                             tma_load_4d(dst + cb * (BN * 128), &tmap_k, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS,
-                                        w.h, u * BN, w.b, pol_kv);
+                                        w.h / p.group, u * BN, w.b, pol_kv);
                     }
                     if (with_v) {
 #pragma unroll
                         for (int cb = 0; cb < Cfg::NCB; ++cb)
                             tma_load_4d(dst + Cfg::KV_TILE_BYTES + cb * (BN * 128), &tmap_v, &bars->ring_full[stage],
-                                        cb * Cfg::BOX_ELEMS, w.h, (u - 1) * BN, w.b, pol_kv);
+                                        cb * Cfg::BOX_ELEMS, w.h / p.group, (u - 1) * BN, w.b, pol_kv);
                     }
                     ++it;
                 }
@@ -567,8 +568,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const int khi = p.causal ? min(i, p.N - 1) : p.N - 1;
             float vmax = 1.0f;
             float q_mult = p.scale_log2;
+            // Key/value head of this query head (grouped-query attention).
+            const int bh_kv = b * (p.H / p.group) + h / p.group;
             if constexpr (Cfg::FP8) {
-                const float* vs = p.v_scale + static_cast<size_t>(bh) * nblk;
+                const float* vs = p.v_scale + static_cast<size_t>(bh_kv) * nblk;
                 vmax = 0.0f;
                 for (int x = 0; x < nblk; ++x) vmax = fmaxf(vmax, vs[x]);
                 if (!(vmax > 0.0f)) vmax = 1.0f;
@@ -588,7 +591,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 float mult = q_mult;
                 float pv_mult = 1.0f;
                 if constexpr (Cfg::FP8) {
-                    const size_t sb = static_cast<size_t>(bh) * nblk + (j * BN) / 128;
+                    const size_t sb = static_cast<size_t>(bh_kv) * nblk + (j * BN) / 128;
                     mult *= p.k_scale[sb];
                     pv_mult = 256.0f * (p.v_scale[sb] / vmax);
                 }

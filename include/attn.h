@@ -89,6 +89,25 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float*
                  void* stream);
 
 /*
+ * attn_fwd_gqa / attn_fwd_fp8_gqa -- grouped-query and multi-query attention
+ * (deep-reading report §3.4: FA3 keeps FA2's index adjustment for MQA/GQA,
+ * so K and V are not duplicated in memory).  As attn_fwd / attn_fwd_fp8,
+ * except that K and V (and, for FP8, k_scale and v_scale) have H_kv heads:
+ *   k, v (k8, v8)       : (B, N, H_kv, d)
+ *   k_scale, v_scale    : float32 (B, H_kv, ceil(N / 128))
+ * H_kv must divide H; query head h reads key/value head h / (H / H_kv).
+ * H_kv == H is multi-head attention (attn_fwd and attn_fwd_fp8 call these
+ * with H_kv = H); H_kv == 1 is multi-query attention.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int H_kv, int N, int d, int causal, float scale, int window,
+                 void* stream);
+int attn_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o, float* lse,
+                     int B, int H, int H_kv, int N, int d, int causal, float scale, int window,
+                     const float* q_scale, const float* k_scale, const float* v_scale,
+                     void* stream);
+
+/*
  * attn_fp8_prep -- fused rotation + block quantisation of one tensor
  * (deep-reading report §2.2 / §3.3).
  *   x      : const bf16 (B, N, H, d)

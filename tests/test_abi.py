@@ -76,3 +76,11 @@ def test_prep_arguments_checked(lib):
 
 def test_wait_limit_setter(lib):
     assert lib.attn_set_wait_limit(0) == 0
+
+
+def test_gqa_head_count_checked(lib):
+    assert lib.attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 6, 4, 16, 128, 0, 0.0, 0, None) == -1
+    assert b"divide" in lib.attn_last_error_string()
+    assert lib.attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 6, 0, 16, 128, 0, 0.0, 0, None) == -1
+    assert lib.attn_fwd_fp8_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 3, 16, 128, 0, 0.0, 0, FAKE, FAKE, FAKE,
+                                None) == -1
