@@ -85,6 +85,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def cublaslt_fp8_peak():
+    """The e4m3 GEMM throughput measured on this GPU type by `--fp8-peak`
+    (stored beside the ncu summaries), for context beside the nominal-ratio
+    denominator; None when absent."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "fp8_gemm_peak.json")) as f:
+            return json.load(f).get("fp8_tflops")
+    except (OSError, ValueError):
+        return None
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_71_gb300", "csrc")
@@ -265,6 +276,54 @@ def run_reference(args, w, key):
     print(json.dumps(line), flush=True)
 
 
+def measure_fp8_peak():
+    """Dense e4m3 GEMM throughput of cuBLASLt (torch._scaled_mm, 8192^3,
+    bf16 output), measured like the bf16 peak: best of 10 (burst) and back to
+    back for 4 s (sustained)."""
+    import torch
+    n = 8192
+    a = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn).t()
+    one = torch.ones((), device="cuda")
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    flops = 2.0 * n ** 3
+    with ClockSampler(None) as clk:
+        t0 = time.perf_counter()
+        cnt = 0
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        while time.perf_counter() - t0 < 4.0:
+            for _ in range(20):
+                mm()
+            cnt += 20
+            torch.cuda.synchronize()
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+    out = {"fp8_tflops": round(flops / (best / 1e3) / 1e12, 1),
+           "fp8_tflops_sustained": round(flops * cnt / (ms / 1e3) / 1e12, 1),
+           "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3 (2 N^3): best of 10 (burst) and back to back "
+                  "for 4 s (sustained), CUDA events", "clocks": clk.summary(),
+           "gpu": torch.cuda.get_device_name(0), "torch": torch.__version__}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -274,7 +333,11 @@ def main():
     ap.add_argument("--workload", default="c2")
     ap.add_argument("--quick", action="store_true", help="skip e2e, FP8 and CPU baseline (profiling runs)")
     ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--fp8-peak", action="store_true", help="measure the cuBLASLt e4m3 GEMM peak and exit")
     args = ap.parse_args()
+    if args.fp8_peak:
+        measure_fp8_peak()
+        return
     w = workload(args.workload)
     if args.impl == "reference":
         run_reference(args, w, args.workload)
@@ -368,6 +431,8 @@ def main():
             "peak_source": peak_note,
             "frac_of_sustained": round(achieved / (peaks.get("bf16_tflops_sustained", peak) *
                                                    (2.0 if w["dtype"] == "fp8" else 1.0)), 4)}
+    if w["dtype"] == "fp8" and cublaslt_fp8_peak():
+        roof["frac_of_cublaslt_fp8_gemm"] = round(achieved / cublaslt_fp8_peak(), 4)
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w["dtype"] == "bf16" else "e4m3", "data": "synthetic",
@@ -462,6 +527,9 @@ def fp8_secondary(api, device, stream, steps):
     out["frac_of_fp8_peak"] = round(out["fwd"]["tflops"] / fp8_peak, 4)
     out["fp8_peak"] = fp8_peak
     out["fp8_peak_source"] = f"{src} bf16 burst x 2 (nominal fp8:bf16 ratio)"
+    if cublaslt_fp8_peak():
+        out["frac_of_cublaslt_fp8_gemm"] = round(out["fwd"]["tflops"] / cublaslt_fp8_peak(), 4)
+        out["cublaslt_fp8_gemm_tflops"] = cublaslt_fp8_peak()
     return out
 
 
