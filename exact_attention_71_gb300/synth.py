@@ -144,3 +144,14 @@ def sample_rows(N: int, count: int, seed: int, must=()) -> np.ndarray:
             rows.add(int(min(x, N - 1)))
         k += 4 * count
     return np.array(sorted(rows), dtype=np.int32)
+
+
+def rope_tables(N: int, d: int, base: float = 10000.0):
+    """Rotary-embedding tables for token positions 0..N-1: cos and sin of the
+    angle n * base^(-2i/d) for pair index i < d/2, evaluated in float64 and
+    rounded to binary32; shape (N, d/2) each.  (The frequencies of Su et al.,
+    "RoFormer", 2021.)  These are inputs of the RoPE prep, like Q and K."""
+    i = np.arange(d // 2, dtype=np.float64)
+    inv_freq = base ** (-2.0 * i / d)
+    ang = np.arange(N, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)

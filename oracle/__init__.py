@@ -56,6 +56,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_signs.restype = None
             L.oracle_fp8_quantize.argtypes = [P, P, P, P, i, i, i, i, i, i, u64, i, i]
             L.oracle_fp8_quantize.restype = i
+            L.oracle_fp8_quantize_rope.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, u64, i, i]
+            L.oracle_fp8_quantize_rope.restype = i
+            L.oracle_rope_bf16.argtypes = [P, P, P, P, i, i, i, i, i, i]
+            L.oracle_rope_bf16.restype = i
             _lib = L
     return _lib
 
@@ -144,20 +148,48 @@ def signs(d: int, seed: int) -> np.ndarray:
 MODE_BLOCK, MODE_BLOCK_HADAMARD, MODE_PER_TENSOR = 0, 1, 2
 
 
-def fp8_quantize(x, mode, seed=0, is_v=False, block_rows=128, return_rotated=False, nthreads=0):
+def _rope_tables(rope, N, d):
+    cos_t, sin_t, interleaved = rope
+    cos_t = np.ascontiguousarray(cos_t, dtype=np.float32)
+    sin_t = np.ascontiguousarray(sin_t, dtype=np.float32)
+    if cos_t.shape != (N, d // 2) or sin_t.shape != (N, d // 2):
+        raise ValueError("RoPE tables must be (N, d/2)")
+    return cos_t, sin_t, int(bool(interleaved))
+
+
+def rope(x, cos_t, sin_t, interleaved=False, nthreads=0):
+    """RoPE of a (B, N, H, d) bf16 tensor (uint16 bits) with binary32 tables
+    (N, d/2); returns float32 (B, N, H, d)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    B, N, H, d = x.shape
+    c, s, il = _rope_tables((cos_t, sin_t, interleaved), N, d)
+    out = np.empty(x.shape, dtype=np.float32)
+    if lib().oracle_rope_bf16(_ptr(x), _ptr(out), _ptr(c), _ptr(s), B, N, H, d, il, int(nthreads)) != 0:
+        raise ValueError("oracle_rope: bad arguments")
+    return out
+
+
+def fp8_quantize(x, mode, seed=0, is_v=False, block_rows=128, return_rotated=False, nthreads=0, rope=None):
     """FP8 prep of one (B, N, H, d) bf16 tensor (uint16 bits).
 
+    rope: optional (cos, sin, interleaved) with binary32 tables (N, d/2);
+    RoPE is then applied before the rotation and the quantiser (Q, K only).
     Returns (codes uint8 (B,N,H,d), scales float32 (B,H,nblk)[, rotated f32]).
     """
     x = np.ascontiguousarray(x, dtype=np.uint16)
     B, N, H, d = x.shape
+    rc_, rs_, ril = (None, None, 0)
+    if rope is not None:
+        rc_, rs_, ril = _rope_tables(rope, N, d)
     nblk = (N + block_rows - 1) // block_rows
     codes = np.empty(x.shape, dtype=np.uint8)
     scales = np.empty((B, H, nblk), dtype=np.float32)
     rot = np.empty(x.shape, dtype=np.float32) if return_rotated else None
-    rc = lib().oracle_fp8_quantize(_ptr(x), _ptr(codes), _ptr(scales),
-                                   _ptr(rot) if rot is not None else None,
-                                   B, H, N, d, block_rows, mode, seed, int(bool(is_v)), int(nthreads))
+    rc = lib().oracle_fp8_quantize_rope(_ptr(x), _ptr(codes), _ptr(scales),
+                                        _ptr(rot) if rot is not None else None,
+                                        _ptr(rc_) if rc_ is not None else None,
+                                        _ptr(rs_) if rs_ is not None else None, ril,
+                                        B, H, N, d, block_rows, mode, seed, int(bool(is_v)), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_fp8_quantize: bad arguments")
     if return_rotated:

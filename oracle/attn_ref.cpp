@@ -38,6 +38,20 @@
 // 4 exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is
 // NaN, largest finite 448) defines the encoder below.
 //
+// Rotary position embedding before the quantiser (the report's §2.2 and
+// §3.3: the block quantisation can ride inside the memory-bound rotary
+// embedding kernel).  RoPE itself is the rotation of Su et al., "RoFormer:
+// Enhanced Transformer with Rotary Position Embedding" (2021): the pair
+// (a, b) of token n and pair index i turns by the angle of table entry
+// (n, i):  a' = a cos - b sin,  b' = a sin + b cos.  Pairs are (i, i + d/2)
+// ("half-split") or (2i, 2i + 1) ("interleaved").  The caller supplies the
+// binary32 cos / sin tables, shape (N, d/2).  The rotation is evaluated in
+// binary32 with each product and each sum rounded (no fused multiply-add),
+// the precision the CUDA path computes it in, because its result feeds the
+// quantisation decision.  Order on Q and K: RoPE, then the Hadamard rotation,
+// then the quantiser (x R_n M: M acts on the already position-rotated row,
+// and (q R_m M)(k R_n M)^T = (q R_m)(k R_n)^T).
+//
 // Random signs of D: bit 63 of successive outputs of splitmix64 seeded with
 // the caller's seed (Steele, Lea and Flood 2014; Vigna's public reference
 // splitmix64.c): output c (c = 0, 1, ...) is mix(seed + (c + 1) * gamma).
@@ -300,15 +314,46 @@ void oracle_signs(int d, unsigned long long seed, double* out) {
     for (long c = 0; c < d; ++c) out[c] = sign_of(seed, c);
 }
 
+// RoPE of one row of token n (binary32 in, binary32 out, in place).
+static void rope_row(float* r, long n, int d, const float* cos_t, const float* sin_t, int interleaved) {
+    const long half = d / 2;
+    for (long i = 0; i < half; ++i) {
+        const long ia = interleaved ? 2 * i : i;
+        const long ib = interleaved ? 2 * i + 1 : i + half;
+        const float c = cos_t[n * half + i], s = sin_t[n * half + i];
+        const float a = r[ia], b = r[ib];
+        const float ac = a * c, bs = b * s, as = a * s, bc = b * c;   // each rounded
+        r[ia] = ac - bs;
+        r[ib] = as + bc;
+    }
+}
+
+// x: bf16 (B, N, H, d) -> out: binary32 RoPE(x), same layout.
+int oracle_rope_bf16(const uint16_t* x, float* out, const float* cos_t, const float* sin_t,
+                     int B, int N, int H, int d, int interleaved, int nthreads) {
+    if (B < 0 || N < 0 || H < 0 || d <= 0 || (d & 1)) return -1;
+    parallel_for(static_cast<long>(B) * N * H, nthreads, [&](long row) {
+        const long n = (row / H) % N;
+        float* r = out + row * d;
+        for (long c = 0; c < d; ++c) r[c] = static_cast<float>(bf16_value(x[row * d + c]));
+        rope_row(r, n, d, cos_t, sin_t, interleaved);
+    });
+    return 0;
+}
+
 // x: bf16 (B, N, H, d).  x8: e4m3 codes (B, N, H, d).  scales: float
-// (B, H, ceil(N / block_rows)).  rotated (optional): the binary32 values r
+// (B, H, ceil(N / block_rows)).  rope_cos / rope_sin: optional binary32
+// tables (N, d/2); when given, RoPE is applied first (Q and K only).  rotated (optional): the binary32 values r
 // that were quantised, (B, N, H, d).
 // mode 0: per-block scales; 1: per-block scales after the rotation (not for
 // V); 2: one scale for the whole tensor (written to every block entry).
-int oracle_fp8_quantize(const uint16_t* x, uint8_t* x8, float* scales, float* rotated,
-                        int B, int H, int N, int d, int block_rows, int mode,
-                        unsigned long long seed, int is_v, int nthreads) {
+int oracle_fp8_quantize_rope(const uint16_t* x, uint8_t* x8, float* scales, float* rotated,
+                             const float* rope_cos, const float* rope_sin, int rope_interleaved,
+                             int B, int H, int N, int d, int block_rows, int mode,
+                             unsigned long long seed, int is_v, int nthreads) {
     if (B < 0 || H < 0 || N < 0 || d <= 0 || block_rows <= 0 || mode < 0 || mode > 2) return -1;
+    const bool rope = rope_cos != nullptr;
+    if (rope && (is_v || (d & 1) || rope_sin == nullptr)) return -1;
     const bool rotate = (mode == 1) && !is_v;
     if (rotate && !is_pow2(d)) return -1;
     const long nblk = (N + block_rows - 1) / block_rows;
@@ -319,17 +364,21 @@ int oracle_fp8_quantize(const uint16_t* x, uint8_t* x8, float* scales, float* ro
         M.resize(static_cast<size_t>(d) * d);
         oracle_rotation_matrix(d, seed, M.data());
     }
-    // r = x M (double sum, rounded once to binary32) or r = x.
+    // u = RoPE(x) (binary32) or u = x;  r = u M (double sum, rounded once to
+    // binary32) or r = u.
     parallel_for(static_cast<long>(B) * N * H, nthreads, [&](long row) {
         const uint16_t* xr = x + row * d;
         float* rr = r.data() + row * d;
+        std::vector<float> u(d);
+        for (long c = 0; c < d; ++c) u[c] = static_cast<float>(bf16_value(xr[c]));
+        if (rope) rope_row(u.data(), (row / H) % N, d, rope_cos, rope_sin, rope_interleaved);
         if (!rotate) {
-            for (long c = 0; c < d; ++c) rr[c] = static_cast<float>(bf16_value(xr[c]));
+            for (long c = 0; c < d; ++c) rr[c] = u[c];
             return;
         }
         for (long c = 0; c < d; ++c) {
             double acc = 0.0;
-            for (long t = 0; t < d; ++t) acc += bf16_value(xr[t]) * M[t * d + c];
+            for (long t = 0; t < d; ++t) acc += static_cast<double>(u[t]) * M[t * d + c];
             rr[c] = static_cast<float>(acc);
         }
     });
@@ -364,6 +413,13 @@ int oracle_fp8_quantize(const uint16_t* x, uint8_t* x8, float* scales, float* ro
     });
     if (rotated) std::memcpy(rotated, r.data(), sizeof(float) * total);
     return 0;
+}
+
+int oracle_fp8_quantize(const uint16_t* x, uint8_t* x8, float* scales, float* rotated,
+                        int B, int H, int N, int d, int block_rows, int mode,
+                        unsigned long long seed, int is_v, int nthreads) {
+    return oracle_fp8_quantize_rope(x, x8, scales, rotated, nullptr, nullptr, 0, B, H, N, d, block_rows,
+                                    mode, seed, is_v, nthreads);
 }
 
 }  // extern "C"
