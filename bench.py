@@ -96,13 +96,21 @@ def cublaslt_fp8_peak():
         return None
 
 
-def kernel_source_hash() -> str:
+# The sources each timed kernel is compiled from: a recorded DRAM traffic
+# figure is used only while these files are unchanged.
+KERNEL_SOURCES = {
+    "attn_fwd": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_bf16_d128.cu"),
+    "attn_fwd_fp8": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d128.cu"),
+    "fp8_prep": ("fp8_prep.cu", "fp8_prep.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str = "attn_fwd") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_71_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -116,7 +124,7 @@ def recorded_traffic(kernel: str, workload_key: str):
     except Exception:
         return None
     ent = rec.get(f"{kernel}/{workload_key}")
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 

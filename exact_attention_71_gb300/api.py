@@ -52,6 +52,8 @@ def library() -> ctypes.CDLL:
         L.attn_fwd_fp8_gqa.argtypes = [P, P, P, P, P, i, i, i, i, i, i, f, i, P, P, P, P]
         L.attn_fwd_fp8_gqa.restype = i
         L.attn_fp8_prep.argtypes = [P, P, P, i, i, i, i, i, i, u64, i, P]
+        L.attn_fp8_prep_rope.argtypes = [P, P, P, P, P, i, i, i, i, i, i, u64, i, P]
+        L.attn_fp8_prep_rope.restype = i
         L.attn_fp8_prep.restype = i
         L.attn_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         L.attn_device_status.restype = i
@@ -181,10 +183,44 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, sc
     return out, lse
 
 
-def fp8_prepare_qkv(q, k, v, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0, stream=None):
-    """Runs the prep on Q, K (rotated in mode 1) and V (never rotated)."""
-    q8, qs = attn_fp8_prep(q, mode, sign_seed, False, stream=stream)
-    k8, ks = attn_fp8_prep(k, mode, sign_seed, False, stream=stream)
+def attn_fp8_prep_rope(x, rope_cos, rope_sin, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0,
+                       interleaved: bool = False, out=None, scales=None, stream=None):
+    """RoPE fused with the FP8 prep of Q or K: each row of token n is turned
+    by the (N, d/2) float32 cos / sin tables (pairs (i, i + d/2), or (2i, 2i+1)
+    when interleaved), then rotated (mode 1) and block-quantised.
+
+    Returns (codes uint8 (B,N,H,d), scales float32 (B,H,ceil(N/128))).
+    """
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 4 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 (B, N, H, d) CUDA tensor")
+    B, N, H, d = x.shape
+    for t in (rope_cos, rope_sin):
+        if (not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.shape != (N, d // 2)
+                or t.device != x.device):
+            raise ValueError("rope_cos / rope_sin must be contiguous float32 (N, d/2) tensors on x's device")
+    nblk = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((B, H, nblk), dtype=torch.float32, device=x.device)
+    rc = library().attn_fp8_prep_rope(_ptr(x), _ptr(out), _ptr(scales), _ptr(rope_cos), _ptr(rope_sin),
+                                      B, H, N, d, BLOCK_ROWS, int(mode), int(sign_seed) & 0xFFFFFFFFFFFFFFFF,
+                                      int(bool(interleaved)), ctypes.c_void_p(_stream(stream)))
+    _check("attn_fp8_prep_rope", rc)
+    return out, scales
+
+
+def fp8_prepare_qkv(q, k, v, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0, stream=None, rope=None):
+    """Runs the prep on Q, K (rotated in mode 1) and V (never rotated).
+    rope: optional (cos, sin, interleaved); RoPE is then fused into the prep
+    of Q and K."""
+    if rope is None:
+        q8, qs = attn_fp8_prep(q, mode, sign_seed, False, stream=stream)
+        k8, ks = attn_fp8_prep(k, mode, sign_seed, False, stream=stream)
+    else:
+        c, s_, il = rope
+        q8, qs = attn_fp8_prep_rope(q, c, s_, mode, sign_seed, il, stream=stream)
+        k8, ks = attn_fp8_prep_rope(k, c, s_, mode, sign_seed, il, stream=stream)
     v8, vs = attn_fp8_prep(v, mode, sign_seed, True, stream=stream)
     return q8, k8, v8, qs, ks, vs
 

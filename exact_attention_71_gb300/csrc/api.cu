@@ -235,9 +235,27 @@ int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, i
     if (!x || !x8 || !scales) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(x) || !aligned16(x8) || !aligned16(scales))
         return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-    cudaError_t e = attn::run_fp8_prep(x, x8, scales, B, H, N, d, mode, sign_seed, is_v != 0,
+    cudaError_t e = attn::run_fp8_prep(x, x8, scales, B, H, N, d, mode, sign_seed, is_v != 0, nullptr, nullptr, 0,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_fp8_prep launch");
+    return ATTN_OK;
+}
+
+int attn_fp8_prep_rope(const void* x, void* x8, float* scales, const float* rope_cos, const float* rope_sin,
+                       int B, int H, int N, int d, int block_rows, int mode, unsigned long long sign_seed,
+                       int interleaved, void* stream) {
+    g_err[0] = '\0';
+    if (B < 0 || H < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d N=%d)", B, H, N);
+    if (d != 64 && d != 128 && d != 256) return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128, 256)", d);
+    if (block_rows != 128) return fail(ATTN_ERR_UNSUPPORTED, "block_rows must be 128 (got %d)", block_rows);
+    if (mode < 0 || mode > 2) return fail(ATTN_ERR_INVALID_ARG, "mode %d (0, 1 or 2)", mode);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    if (!x || !x8 || !scales || !rope_cos || !rope_sin) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(x8) || !aligned16(scales) || !aligned16(rope_cos) || !aligned16(rope_sin))
+        return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    cudaError_t e = attn::run_fp8_prep(x, x8, scales, B, H, N, d, mode, sign_seed, false, rope_cos, rope_sin,
+                                       interleaved ? 2 : 1, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_fp8_prep_rope launch");
     return ATTN_OK;
 }
 

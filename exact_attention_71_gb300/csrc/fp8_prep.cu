@@ -8,6 +8,13 @@
 // device-memory bandwidth).  A warp holds whole rows: lane l keeps elements
 // [l*E, l*E + E) of a row, E = d / 32.  The Walsh-Hadamard butterflies with
 // stride < E stay inside a thread; the wider ones pair lanes with shuffles.
+// With RoPE (rotary position embedding; Su et al., "RoFormer", 2021) the
+// row is first turned pair by pair with the caller's binary32 cos / sin
+// tables (N, d/2): a' = a cos - b sin, b' = a sin + b cos, each product and
+// sum rounded (no FMA), pairs (i, i + d/2) ("half-split": the partner sits
+// 16 lanes away) or (2i, 2i + 1) ("interleaved": inside the thread).  This is
+// the placement the report's §2.2 names: quantisation riding inside the
+// memory-bound rotary-embedding pass.
 // Mode 2 (one scale per tensor) runs three launches: block amax into
 // `scales`, a one-CTA reduction that turns them into the tensor's scale,
 // and the quantisation with that scale.
@@ -34,6 +41,29 @@ __device__ __forceinline__ float diag_sign(unsigned long long seed, int c) {
 }
 
 enum Pass { kFused = 0, kAmaxOnly = 1, kApplyScale = 2 };
+enum Rope { kNoRope = 0, kRopeHalf = 1, kRopeInterleaved = 2 };
+
+template <int K> struct FloatVec;
+template <> struct FloatVec<1> { using T = float; };
+template <> struct FloatVec<2> { using T = float2; };
+template <> struct FloatVec<4> { using T = float4; };
+template <> struct FloatVec<8> { using T = float4; };   // loaded as two float4
+
+// K consecutive floats from a 4*K-byte aligned address.
+template <int K>
+__device__ __forceinline__ void load_floats(const float* __restrict__ p, float (&out)[K]) {
+    if constexpr (K == 8) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+        out[4] = b.x; out[5] = b.y; out[6] = b.z; out[7] = b.w;
+    } else {
+        const typename FloatVec<K>::T v = __ldg(reinterpret_cast<const typename FloatVec<K>::T*>(p));
+        const float* f = reinterpret_cast<const float*>(&v);
+#pragma unroll
+        for (int k = 0; k < K; ++k) out[k] = f[k];
+    }
+}
 
 // x / s rounded to nearest for s > 0, from the correctly rounded reciprocal
 // and one residual correction (Markstein, "Computation of elementary
@@ -52,11 +82,14 @@ template <> struct RowLoad<2> { using T = uint32_t; };
 template <> struct RowLoad<4> { using T = uint2; };
 template <> struct RowLoad<8> { using T = uint4; };
 
-template <int D, int WARPS, int PASS>
+template <int D, int WARPS, int PASS, int ROPE>
 __global__ void __launch_bounds__(WARPS * 32)
     fp8_prep_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ x8, float* __restrict__ scales,
-                    int H, int N, int nblk, int rotate, unsigned long long seed) {
+                    int H, int N, int nblk, int rotate, unsigned long long seed,
+                    const float* __restrict__ rope_cos, const float* __restrict__ rope_sin) {
     constexpr int E = D / 32;                     // elements per lane
+    // table entries a lane needs per row: E (half-split) or E/2 (interleaved)
+    constexpr int TE = ROPE == kRopeInterleaved ? E / 2 : E;
     constexpr int RPW = kBlockRows / WARPS;       // rows per warp
     using Raw = typename RowLoad<E>::T;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -77,6 +110,22 @@ __global__ void __launch_bounds__(WARPS * 32)
         }
     }
 
+    // RoPE table entries of this lane's pairs: loaded up front for all rows
+    // where the registers allow it (d <= 128), else row by row.
+    constexpr bool PRELOAD = ROPE != kNoRope && D <= 128;
+    constexpr int TROWS = PRELOAD ? RPW : 1;
+    const int i0 = ROPE == kRopeHalf ? (lane & 15) * E : lane * (E / 2);   // first pair index
+    float tc[TROWS][TE], ts[TROWS][TE];
+    auto load_table = [&](int rr, int slot) {
+        const int n = min(n0 + rr, N - 1);
+        load_floats<TE>(rope_cos + static_cast<size_t>(n) * (D / 2) + i0, tc[slot]);
+        load_floats<TE>(rope_sin + static_cast<size_t>(n) * (D / 2) + i0, ts[slot]);
+    };
+    if constexpr (PRELOAD) {
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) load_table(rr, rr);
+    }
+
     float sgn[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) sgn[e] = rotate ? diag_sign(seed, lane * E + e) : 1.0f;
@@ -90,6 +139,28 @@ __global__ void __launch_bounds__(WARPS * 32)
         for (int k = 0; k < E / 2; ++k) {
             r[rr][2 * k] = __bfloat162float(pv[k].x);
             r[rr][2 * k + 1] = __bfloat162float(pv[k].y);
+        }
+        const int slot = PRELOAD ? rr : 0;
+        if constexpr (ROPE != kNoRope && !PRELOAD) load_table(rr, 0);
+        if constexpr (ROPE == kRopeHalf) {
+            // lanes 0-15 hold the first halves a, lanes 16-31 the partners b
+            const bool upper = lane >= 16;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float other = __shfl_xor_sync(0xffffffffu, r[rr][e], 16);
+                const float a = upper ? other : r[rr][e], bb = upper ? r[rr][e] : other;
+                const float c = tc[slot][e], sn = ts[slot][e];
+                r[rr][e] = upper ? __fadd_rn(__fmul_rn(a, sn), __fmul_rn(bb, c))
+                                 : __fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn));
+            }
+        } else if constexpr (ROPE == kRopeInterleaved) {
+#pragma unroll
+            for (int k = 0; k < E / 2; ++k) {
+                const float a = r[rr][2 * k], bb = r[rr][2 * k + 1];
+                const float c = tc[slot][k], sn = ts[slot][k];
+                r[rr][2 * k] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn));
+                r[rr][2 * k + 1] = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(bb, c));
+            }
         }
         if (rotate) {
 #pragma unroll
@@ -196,9 +267,10 @@ __global__ void __launch_bounds__(1024) per_tensor_scale_kernel(float* scales, l
     for (long long i = threadIdx.x; i < count; i += blockDim.x) scales[i] = s;
 }
 
-template <int D, int WARPS>
+template <int D, int WARPS, int ROPE>
 cudaError_t launch_prep(const void* x, void* x8, float* scales, int B, int H, int N, int mode,
-                        unsigned long long seed, bool is_v, cudaStream_t stream) {
+                        unsigned long long seed, bool is_v, const float* rope_cos, const float* rope_sin,
+                        cudaStream_t stream) {
     const int nblk = (N + kBlockRows - 1) / kBlockRows;
     const long long ctas = static_cast<long long>(B) * H * nblk;
     if (ctas >= (1ll << 31)) return cudaErrorInvalidValue;
@@ -207,23 +279,50 @@ cudaError_t launch_prep(const void* x, void* x8, float* scales, int B, int H, in
     const int rotate = (mode == 1 && !is_v) ? 1 : 0;
     const dim3 grid(static_cast<unsigned>(ctas)), block(WARPS * 32);
     if (mode != 2) {
-        fp8_prep_kernel<D, WARPS, kFused><<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, rotate, seed);
+        fp8_prep_kernel<D, WARPS, kFused, ROPE>
+            <<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, rotate, seed, rope_cos, rope_sin);
         return cudaGetLastError();
     }
-    fp8_prep_kernel<D, WARPS, kAmaxOnly><<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, 0, seed);
+    fp8_prep_kernel<D, WARPS, kAmaxOnly, ROPE>
+        <<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, 0, seed, rope_cos, rope_sin);
     per_tensor_scale_kernel<<<1, 1024, 0, stream>>>(scales, ctas);
-    fp8_prep_kernel<D, WARPS, kApplyScale><<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, 0, seed);
+    fp8_prep_kernel<D, WARPS, kApplyScale, ROPE>
+        <<<grid, block, 0, stream>>>(xb, q8, scales, H, N, nblk, 0, seed, rope_cos, rope_sin);
     return cudaGetLastError();
+}
+
+template <int D, int WARPS>
+cudaError_t launch_prep_any(const void* x, void* x8, float* scales, int B, int H, int N, int mode,
+                            unsigned long long seed, bool is_v, const float* rope_cos, const float* rope_sin,
+                            int rope, cudaStream_t stream) {
+    switch (rope) {
+        case kNoRope:
+            return launch_prep<D, WARPS, kNoRope>(x, x8, scales, B, H, N, mode, seed, is_v, nullptr, nullptr, stream);
+        case kRopeHalf:
+            return launch_prep<D, WARPS, kRopeHalf>(x, x8, scales, B, H, N, mode, seed, is_v, rope_cos, rope_sin,
+                                                    stream);
+        case kRopeInterleaved:
+            return launch_prep<D, WARPS, kRopeInterleaved>(x, x8, scales, B, H, N, mode, seed, is_v, rope_cos,
+                                                           rope_sin, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
 
 cudaError_t run_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, int d, int mode,
-                         unsigned long long sign_seed, bool is_v, cudaStream_t stream) {
+                         unsigned long long sign_seed, bool is_v, const float* rope_cos, const float* rope_sin,
+                         int rope, cudaStream_t stream) {
     switch (d) {
-        case 64: return launch_prep<64, 16>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
-        case 128: return launch_prep<128, 16>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
-        case 256: return launch_prep<256, 32>(x, x8, scales, B, H, N, mode, sign_seed, is_v, stream);
+        case 64:
+            return launch_prep_any<64, 16>(x, x8, scales, B, H, N, mode, sign_seed, is_v, rope_cos, rope_sin, rope,
+                                           stream);
+        case 128:
+            return launch_prep_any<128, 16>(x, x8, scales, B, H, N, mode, sign_seed, is_v, rope_cos, rope_sin, rope,
+                                            stream);
+        case 256:
+            return launch_prep_any<256, 32>(x, x8, scales, B, H, N, mode, sign_seed, is_v, rope_cos, rope_sin, rope,
+                                            stream);
         default: return cudaErrorInvalidValue;
     }
 }

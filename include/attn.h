@@ -132,6 +132,27 @@ int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, i
                   void* stream);
 
 /*
+ * attn_fp8_prep_rope -- rotary position embedding fused with the FP8 prep of
+ * Q or K (deep-reading report §2.2 / §3.3: the block quantisation costs
+ * nothing extra when it rides inside the memory-bound rotary-embedding
+ * pass).  As attn_fp8_prep with is_v = 0, except that each row of token n is
+ * first turned by RoPE (Su et al., "RoFormer", 2021):
+ *     a' = a cos(n, i) - b sin(n, i),   b' = a sin(n, i) + b cos(n, i)
+ * for pair index i < d/2, with the pair (a, b) = elements (i, i + d/2) when
+ * interleaved == 0 ("half-split") or (2i, 2i + 1) when interleaved != 0.
+ * The products and sums are float32, each rounded (no fused multiply-add).
+ * Then, in this order, the Hadamard rotation (mode 1) and the quantiser.
+ *   rope_cos, rope_sin : const float32 (N, d/2), device, 16-byte aligned,
+ *                        owned by the caller; row n serves token n of every
+ *                        batch and head.
+ * Errors: as attn_fp8_prep; a NULL or unaligned table is
+ * ATTN_ERR_INVALID_ARG.
+ */
+int attn_fp8_prep_rope(const void* x, void* x8, float* scales, const float* rope_cos,
+                       const float* rope_sin, int B, int H, int N, int d, int block_rows,
+                       int mode, unsigned long long sign_seed, int interleaved, void* stream);
+
+/*
  * attn_device_status -- waits for `stream`, then reads and clears the
  * library's device status word.  Every wait inside the kernels is bounded;
  * a kernel that gives up records the site in this word and returns instead

@@ -57,3 +57,40 @@ def assert_bf16_parity(e, label=""):
         assert e["max_excess"] <= BF16_MAX_ABS, msg
         print(f"[cast floor] {label}: max-abs {e['max_abs']:.3e} exceeds 1e-2 only through the bf16 "
               f"output rounding (error beyond half an ulp {e['max_excess']:.3e})")
+
+
+def assert_codes_match_up_to_midpoints(c_gpu, c_ref, s_ref, rot, block_rows=128, max_frac=1e-3):
+    """e4m3 codes of a rotated tensor: equal to the oracle's, except where the
+    oracle's exact quotient rot / scale lies within 1e-5 (relative) of a
+    rounding midpoint between two e4m3 values -- the float32 butterflies and
+    the oracle's double product may round to either side there -- and then
+    only to a neighbouring code."""
+    import oracle
+    vals = np.unique(np.abs(oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))))
+    mids = (vals[:-1] + vals[1:]) / 2
+    N = c_ref.shape[1]
+    sc = np.repeat(s_ref.transpose(0, 2, 1), block_rows, axis=1)[:, :N]      # (B, N, H)
+    y = rot.astype(np.float64) / sc[..., None]
+    a = np.abs(y).ravel()
+    pos = np.searchsorted(mids, a)
+    near = np.minimum(np.abs(a - mids[np.clip(pos - 1, 0, len(mids) - 1)]),
+                      np.abs(a - mids[np.clip(pos, 0, len(mids) - 1)])) <= 1e-5 * np.maximum(a, 2.0 ** -9)
+    cg, cr = c_gpu.ravel(), c_ref.ravel()
+    same = cg == cr
+    assert np.all(same | near), f"{np.sum(~(same | near))} codes differ away from a rounding midpoint"
+    diff = ~same
+    mg, mr = (cg[diff] & 0x7F).astype(int), (cr[diff] & 0x7F).astype(int)
+    same_sign = (cg[diff] & 0x80) == (cr[diff] & 0x80)
+    assert np.all((np.abs(mg - mr) == 1) & (same_sign | (np.minimum(mg, mr) == 0)))
+    assert diff.mean() < max_frac
+
+
+def dequant(codes, scales, block_rows=128):
+    """e4m3 codes (B,N,H,d) torch tensor x block scales (B,H,nblk) -> float64 values."""
+    import oracle
+    c = codes.cpu().numpy()
+    s = scales.cpu().numpy().astype(np.float64)
+    N = c.shape[1]
+    vals = oracle.e4m3_decode(c.ravel()).reshape(c.shape)
+    sc = np.repeat(s.transpose(0, 2, 1), block_rows, axis=1)[:, :N]
+    return vals * sc[..., None]

@@ -84,3 +84,16 @@ def test_gqa_head_count_checked(lib):
     assert lib.attn_fwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 6, 0, 16, 128, 0, 0.0, 0, None) == -1
     assert lib.attn_fwd_fp8_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 3, 16, 128, 0, 0.0, 0, FAKE, FAKE, FAKE,
                                 None) == -1
+
+
+def test_rope_prep_arguments_checked(lib):
+    f = lib.attn_fp8_prep_rope
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 96, 128, 1, 0, 0, None) == -2       # head_dim
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 128, 64, 1, 0, 0, None) == -2       # block rows
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 128, 128, 5, 0, 0, None) == -1      # mode
+    assert f(FAKE, FAKE, FAKE, None, FAKE, 1, 1, 16, 128, 128, 1, 0, 0, None) == -1      # no cos table
+    assert b"null" in lib.attn_last_error_string()
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert f(FAKE, FAKE, FAKE, FAKE, odd, 1, 1, 16, 128, 128, 1, 0, 0, None) == -1       # unaligned sin
+    assert b"aligned" in lib.attn_last_error_string()
+    assert f(None, None, None, None, None, 0, 1, 16, 128, 128, 1, 0, 0, None) == 0       # empty
