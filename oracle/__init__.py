@@ -44,6 +44,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_attn_fwd_bf16.restype = i
             L.oracle_attn_fwd_f64.argtypes = [P, P, P, P, P, i, i, i, i, i, i, d, i, P, i, i]
             L.oracle_attn_fwd_f64.restype = i
+            L.oracle_attn_bwd_bf16.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, d, i, i]
+            L.oracle_attn_bwd_bf16.restype = i
+            L.oracle_attn_bwd_f64.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, d, i, i]
+            L.oracle_attn_bwd_f64.restype = i
             L.oracle_attn_row_probs_f64.argtypes = [P, P, P, i, i, i, i, i, d, i, i, i, i, P]
             L.oracle_attn_row_probs_f64.restype = i
             L.oracle_e4m3_encode_f64.argtypes = [P, P, lng]
@@ -102,6 +106,34 @@ def attention(q, k, v, causal=False, scale=None, window=0, rows=None, nthreads=0
     if rc != 0:
         raise ValueError("oracle_attn_fwd: bad arguments")
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal=False, scale=None, window=0, nthreads=0):
+    """Gradients of the attention forward in fp64 for the upstream gradient
+    dout = dL/dO.
+
+    q, dout: (B, N, H, d); k, v: (B, N, Hkv, d) (Hkv divides H), either all
+    uint16 bf16 bit patterns or all float64.  Returns (dq, dk, dv) in the
+    shapes of q, k, v (float64).
+    """
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    if q.dtype == np.uint16:
+        fn = lib().oracle_attn_bwd_bf16
+        q, k, v, dout = (np.ascontiguousarray(t, dtype=np.uint16) for t in (q, k, v, dout))
+    else:
+        fn = lib().oracle_attn_bwd_f64
+        q, k, v, dout = (np.ascontiguousarray(t, dtype=np.float64) for t in (q, k, v, dout))
+    dq = np.empty(q.shape, dtype=np.float64)
+    dk = np.empty(k.shape, dtype=np.float64)
+    dv = np.empty(v.shape, dtype=np.float64)
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d,
+            int(bool(causal)), float(scale), int(window), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd: bad arguments")
+    return dq, dk, dv
 
 
 def row_probs(q, k, v, b, h, i, causal=False, scale=None, window=0):

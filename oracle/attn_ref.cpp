@@ -38,6 +38,19 @@
 // 4 exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is
 // NaN, largest finite 448) defines the encoder below.
 //
+// Backward ([R] §3.4 appendix note: FA3 keeps FA2's recompute strategy,
+// five matrix products against the forward's two).  With L a scalar loss
+// and dO = dL/dO given, the gradients of the same definition are
+//     P_ij  = exp(s_ij - LSE_i)                 (0 for invisible keys)
+//     dP_ij = dO_i . v_j
+//     D_i   = sum_j P_ij dP_ij                  (softmax Jacobian term)
+//     dS_ij = P_ij (dP_ij - D_i)
+//     dQ_i  = scale sum_j dS_ij k_j
+//     dK_j  = scale sum_(h in group) sum_i dS_ij q_i
+//     dV_j  = sum_(h in group) sum_i P_ij dO_i
+// computed in double in two passes: per query row (LSE, D, dQ), then per
+// key row (dK, dV) with P and dS recomputed from the stored LSE and D.
+//
 // Rotary position embedding before the quantiser (the report's §2.2 and
 // §3.3: the block quantisation can ride inside the memory-bound rotary
 // embedding kernel).  RoPE itself is the rotation of Su et al., "RoFormer:
@@ -256,9 +269,104 @@ double sylvester(long r, long c) {
 
 bool is_pow2(long d) { return d > 0 && (d & (d - 1)) == 0; }
 
+// Backward pass 1, one query row i of query head h: LSE_i, D_i and dQ_i.
+template <class In>
+void backward_row(const In& qin, const In& kin, const In& vin, const In& doin, long b, long h, long i,
+                  long N, long d, int causal, double scale, int window, double* dq_row, double* lse_out,
+                  double* D_out) {
+    std::vector<double> p(N), o(d);
+    double lse;
+    attention_row(qin, kin, vin, b, h, i, N, d, causal, scale, window, o.data(), &lse, p.data());
+    std::vector<double> dout(d), dp(N, 0.0);
+    for (long c = 0; c < d; ++c) dout[c] = doin(b, i, h, c);
+    double D = 0.0;
+    for (long j = 0; j < N; ++j) {
+        if (!key_visible(i, j, causal, window)) continue;
+        double acc = 0.0;
+        for (long c = 0; c < d; ++c) acc += dout[c] * vin(b, j, h, c);
+        dp[j] = acc;
+        D += p[j] * acc;
+    }
+    for (long c = 0; c < d; ++c) dq_row[c] = 0.0;
+    for (long j = 0; j < N; ++j) {
+        if (!key_visible(i, j, causal, window)) continue;
+        const double ds = p[j] * (dp[j] - D);
+        for (long c = 0; c < d; ++c) dq_row[c] += ds * kin(b, j, h, c);
+    }
+    for (long c = 0; c < d; ++c) dq_row[c] *= scale;
+    *lse_out = lse;
+    *D_out = D;
+}
+
+// Backward pass 2, one key row j of key/value head hk: dK_j and dV_j summed
+// over the query heads of the group and all query rows.
+template <class In>
+void backward_key(const In& qin, const In& kin, const In& vin, const In& doin, const double* lse,
+                  const double* Dv, long b, long hk, long j, long N, long H, long d, long group, int causal,
+                  double scale, int window, double* dk_row, double* dv_row) {
+    for (long c = 0; c < d; ++c) dk_row[c] = dv_row[c] = 0.0;
+    for (long h = hk * group; h < (hk + 1) * group; ++h) {
+        const double* lse_h = lse + (b * H + h) * N;
+        const double* D_h = Dv + (b * H + h) * N;
+        for (long i = 0; i < N; ++i) {
+            if (!key_visible(i, j, causal, window)) continue;
+            double s = 0.0, dp = 0.0;
+            for (long c = 0; c < d; ++c) {
+                s += qin(b, i, h, c) * kin(b, j, h, c);
+                dp += doin(b, i, h, c) * vin(b, j, h, c);
+            }
+            const double P = std::exp(scale * s - lse_h[i]);
+            const double ds = P * (dp - D_h[i]);
+            for (long c = 0; c < d; ++c) {
+                dk_row[c] += scale * ds * qin(b, i, h, c);
+                dv_row[c] += P * doin(b, i, h, c);
+            }
+        }
+    }
+}
+
+// q, dout, dq: (B, N, H, d); k, v, dk, dv: (B, N, Hkv, d).
+template <class In>
+int run_backward(const In& q, const In& k, const In& v, const In& dout, double* dq, double* dk, double* dv,
+                 int B, int H, int Hkv, int N, int d, int causal, double scale, int window, int nthreads) {
+    if (B < 0 || H < 0 || N < 0 || d <= 0 || Hkv <= 0 || H % Hkv != 0) return -1;
+    const long group = H / Hkv;
+    std::vector<double> lse(static_cast<size_t>(B) * H * N), Dv(static_cast<size_t>(B) * H * N);
+    parallel_for(static_cast<long>(B) * H * N, nthreads, [&](long it) {
+        const long i = it % N, bh = it / N, b = bh / H, h = bh % H;
+        backward_row(q, k, v, dout, b, h, i, N, d, causal, scale, window, dq + ((b * N + i) * H + h) * d,
+                     &lse[it], &Dv[it]);
+    });
+    parallel_for(static_cast<long>(B) * Hkv * N, nthreads, [&](long it) {
+        const long j = it % N, bhk = it / N, b = bhk / Hkv, hk = bhk % Hkv;
+        const long off = ((b * N + j) * Hkv + hk) * d;
+        backward_key(q, k, v, dout, lse.data(), Dv.data(), b, hk, j, N, H, d, group, causal, scale, window,
+                     dk + off, dv + off);
+    });
+    return 0;
+}
+
 }  // namespace
 
 extern "C" {
+
+int oracle_attn_bwd_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout,
+                         double* dq, double* dk, double* dv, int B, int H, int Hkv, int N, int d, int causal,
+                         double scale, int window, int nthreads) {
+    if (Hkv <= 0 || H % Hkv != 0) return -1;
+    const long g = H / Hkv;
+    return run_backward(Bf16Tensor{q, N, H, d, 1}, Bf16Tensor{k, N, Hkv, d, g}, Bf16Tensor{v, N, Hkv, d, g},
+                        Bf16Tensor{dout, N, H, d, 1}, dq, dk, dv, B, H, Hkv, N, d, causal, scale, window, nthreads);
+}
+
+int oracle_attn_bwd_f64(const double* q, const double* k, const double* v, const double* dout, double* dq,
+                        double* dk, double* dv, int B, int H, int Hkv, int N, int d, int causal, double scale,
+                        int window, int nthreads) {
+    if (Hkv <= 0 || H % Hkv != 0) return -1;
+    const long g = H / Hkv;
+    return run_backward(F64Tensor{q, N, H, d, 1}, F64Tensor{k, N, Hkv, d, g}, F64Tensor{v, N, Hkv, d, g},
+                        F64Tensor{dout, N, H, d, 1}, dq, dk, dv, B, H, Hkv, N, d, causal, scale, window, nthreads);
+}
 
 // Q has H heads, K and V have Hkv heads (Hkv divides H).
 int oracle_attn_fwd_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v,
