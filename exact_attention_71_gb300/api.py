@@ -55,6 +55,11 @@ def library() -> ctypes.CDLL:
         L.attn_fp8_prep_rope.argtypes = [P, P, P, P, P, i, i, i, i, i, i, u64, i, P]
         L.attn_fp8_prep_rope.restype = i
         L.attn_fp8_prep.restype = i
+        sz = ctypes.c_size_t
+        L.attn_bwd_workspace_size.argtypes = [i, i, i, i]
+        L.attn_bwd_workspace_size.restype = sz
+        L.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, sz, i, i, i, i, i, i, f, i, P]
+        L.attn_bwd.restype = i
         L.attn_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         L.attn_device_status.restype = i
         L.attn_set_wait_limit.argtypes = [u64]
@@ -132,6 +137,40 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, window: 
                                     ctypes.c_void_p(_stream(stream)))
         _check("attn_fwd_gqa", rc)
     return out, lse
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(library().attn_bwd_workspace_size(B, H, N, d))
+
+
+def attn_bwd(dout, q, k, v, out, lse, causal: bool = False, scale: float | None = None, window: int = 0,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward of attn_fwd: (dq, dk, dv) for the upstream gradient dout.
+
+    q, dout, out: bf16 (B, N, H, d); k, v: bf16 (B, N, H_kv, d); lse: the
+    forward's float32 (B, H, N).  workspace: optional uint8 CUDA tensor of at
+    least bwd_workspace_bytes(B, H, N, d) bytes (allocated per call when
+    omitted).
+    """
+    _check_qkv(q, k, v, torch.bfloat16)
+    for t, name in ((dout, "dout"), (out, "out")):
+        if t.shape != q.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != q.device:
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, N) tensor")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                            _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
+                            int(bool(causal)), float(scale or 0.0), int(window), ctypes.c_void_p(_stream(stream)))
+    _check("attn_bwd", rc)
+    return dq, dk, dv
 
 
 def attn_fp8_prep(x, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0, is_v: bool = False,

@@ -13,6 +13,8 @@
 #include <mutex>
 
 #include "../../include/attn.h"
+#include "attn_bwd.cuh"
+#include "attn_bwd_kernel.cuh"
 #include "attn_launch.cuh"
 #include "fp8_prep.cuh"
 
@@ -256,6 +258,60 @@ int attn_fp8_prep_rope(const void* x, void* x8, float* scales, const float* rope
     cudaError_t e = attn::run_fp8_prep(x, x8, scales, B, H, N, d, mode, sign_seed, false, rope_cos, rope_sin,
                                        interleaved ? 2 : 1, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_fp8_prep_rope launch");
+    return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+    if (B < 0 || H < 0 || N < 0 || d <= 0) return 0;
+    return static_cast<size_t>(attn::bwd_workspace(B, H, N, d).bytes);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int H_kv, int N,
+             int d, int causal, float scale, int window, void* stream) {
+    g_err[0] = '\0';
+    int rc = check_common(q, k, v, o, lse, B, H, N, d, window);
+    if (rc != ATTN_OK) return rc;
+    if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_bwd supports head_dim 128 only (got %d)", d);
+    if (H_kv <= 0 || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    if (!dout || !dq || !dk || !dv || !workspace) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const attn::BwdWorkspace ws = attn::bwd_workspace(B, H, N, d);
+    if (workspace_bytes < static_cast<size_t>(ws.bytes))
+        return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %lld bytes needed",
+                    workspace_bytes, ws.bytes);
+    attn::BwdMaps maps;
+    if ((rc = make_map(&maps.q, q, B, H, N, d, 2, 64)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.dout, dout, B, H, N, d, 2, 64)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.k, k, B, H_kv, N, d, 2, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.v, v, B, H_kv, N, d, 2, 128)) != ATTN_OK) return rc;
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    attn::BwdParams p{};
+    p.lse2 = reinterpret_cast<const float*>(wsb + ws.off_lse2);
+    p.dvec = reinterpret_cast<const float*>(wsb + ws.off_dvec);
+    p.dq_acc = reinterpret_cast<float*>(wsb + ws.off_dq);
+    p.dk = dk;
+    p.dv = dv;
+    p.B = B;
+    p.H = H;
+    p.H_kv = H_kv;
+    p.N = N;
+    p.N_pad = ws.n_pad;
+    p.group = H / H_kv;
+    p.causal = causal ? 1 : 0;
+    p.window = window;
+    p.scale = resolve_scale(scale, d);
+    p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.n_kblocks = (N + 127) / 128;
+    p.wait_limit = g_wait_limit.load();
+    if ((rc = status_ptr(&p.status)) != ATTN_OK) return rc;
+    cudaError_t e = attn::run_bwd_d128(maps, p, o, dout, lse, dq, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
     return ATTN_OK;
 }
 

@@ -1,5 +1,6 @@
 /*
- * attn.h -- C ABI of the GB300 (sm_103a) fused exact-attention forward.
+ * attn.h -- C ABI of the GB300 (sm_103a) fused exact attention (forward,
+ * FP8 prep, backward).
  *
  * What is computed (FlashAttention-3 deep-reading report, "第三层" intro and
  * §3.1-§3.3; "Efficient Attention & FlashAttention", "数学机理"):
@@ -37,6 +38,8 @@
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -151,6 +154,41 @@ int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, i
 int attn_fp8_prep_rope(const void* x, void* x8, float* scales, const float* rope_cos,
                        const float* rope_sin, int B, int H, int N, int d, int block_rows,
                        int mode, unsigned long long sign_seed, int interleaved, void* stream);
+
+/*
+ * attn_bwd_workspace_size / attn_bwd -- backward of attn_fwd / attn_fwd_gqa
+ * (deep-reading report §3.4: FA3 keeps FA2's recompute strategy; five
+ * matrix products against the forward's two).  For a loss L with upstream
+ * gradient dout = dL/dO:
+ *     P_ij = exp(scale q_i . k_j - LSE_i),  dP_ij = dout_i . v_j,
+ *     D_i = dout_i . o_i,  dS_ij = P_ij (dP_ij - D_i),
+ *     dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,
+ *     dv_j = sum_i P_ij dout_i
+ * (sums over visible pairs; dk, dv of a key/value head sum over the query
+ * heads of its group).
+ *   q, dout, o          : const bf16 (B, N, H, d), device; o and lse are the
+ *                         forward's outputs for the same q, k, v and mask
+ *   k, v                : const bf16 (B, N, H_kv, d)
+ *   lse                 : const float32 (B, H, N) from the forward
+ *   dq                  : bf16 (B, N, H, d), written
+ *   dk, dv              : bf16 (B, N, H_kv, d), written
+ *   workspace           : device, at least attn_bwd_workspace_size(B, H, N, d)
+ *                         bytes, 256-byte aligned, owned by the caller; its
+ *                         contents are scratch (overwritten by every call,
+ *                         so calls sharing one workspace must be ordered on
+ *                         one stream)
+ *   B, H, H_kv, N, d, causal, scale, window : as attn_fwd_gqa
+ * Only d = 128 is supported (ATTN_ERR_UNSUPPORTED otherwise).  Three
+ * launches on `stream`: D and the zeroed float32 dQ accumulator, the fused
+ * backward, and the conversion of dQ to bf16.  Errors: as attn_fwd_gqa; a
+ * NULL, unaligned or too small workspace is ATTN_ERR_INVALID_ARG.
+ * attn_bwd_workspace_size returns 0 for negative sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, void* workspace,
+             size_t workspace_bytes, int B, int H, int H_kv, int N, int d, int causal,
+             float scale, int window, void* stream);
 
 /*
  * attn_device_status -- waits for `stream`, then reads and clears the

@@ -15,7 +15,7 @@ HEADER = os.path.join(ROOT, "include", "attn.h")
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(attn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(attn_\w+)\s*\(", text, flags=re.M)))
 
 
 @pytest.fixture(scope="module")
@@ -97,3 +97,20 @@ def test_rope_prep_arguments_checked(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, odd, 1, 1, 16, 128, 128, 1, 0, 0, None) == -1       # unaligned sin
     assert b"aligned" in lib.attn_last_error_string()
     assert f(None, None, None, None, None, 0, 1, 16, 128, 128, 1, 0, 0, None) == 0       # empty
+
+
+def test_backward_arguments_checked(lib):
+    f = lib.attn_bwd
+    ws = lib.attn_bwd_workspace_size(1, 2, 100, 128)
+    # (2 x float32 per padded row) + float32 dQ accumulator, 256-byte aligned parts
+    assert ws == 2 * 1024 + 2 * 128 * 128 * 4
+    assert lib.attn_bwd_workspace_size(-1, 2, 100, 128) == 0
+    args = lambda d=128, hkv=2, wsp=FAKE, wsb=ws: (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, wsp, wsb,
+                                                   1, 2, hkv, 100, d, 1, 0.0, 0, None)
+    assert f(*args(d=64)) == -2
+    assert f(*args(hkv=3)) == -1
+    assert f(*args(wsp=None)) == -1
+    assert f(*args(wsp=ctypes.c_void_p((1 << 20) + 16))) == -1
+    assert b"256-byte" in lib.attn_last_error_string()
+    assert f(*args(wsb=ws - 1)) == -1
+    assert b"smaller" in lib.attn_last_error_string()
