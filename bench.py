@@ -6,10 +6,12 @@ fused forward over the batch (load, QK^T, online softmax, correction, PV and
 epilogue all inside one kernel launch).  The FP8 path (prep of Q, K, V with
 block scales + Hadamard rotation, then the FP8 forward) is measured on its
 own workload (B=2, H=16, N=8192, d=128, non-causal, outlier inputs) and
-reported in the "fp8" object of the same line.
+reported in the "fp8" object of the same line, and the backward on the
+pages' Fig. 6 point (B=1, H=16, N=16384, d=128, non-causal; FLOPs 2.5 x the
+forward's) in its "bwd" object.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c2|c4|c5|c3:N:d:causal] [--quick]
+                    [--workload c2|c4|c5|gqa|bwd|bwd_c2|c3:N:d:causal|bwd:N:causal] [--quick]
 
 Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
 device (weak scaling, no collective on the data path); `value` is the work of
@@ -45,6 +47,12 @@ WORKLOADS = {
                d=128, causal=True, window=4096, dtype="bf16"),
     "gqa": dict(name="bf16 fwd grouped-query B=2 H=32 H_kv=8 N=8192 d=128 causal", B=2, H=32, Hkv=8, N=8192,
                 d=128, causal=True, window=0, dtype="bf16"),
+    # The backward's headline point on the pages (Fig. 6: d=128, 16k tokens,
+    # hidden 2048, non-causal N=16k) and the forward's headline shape.
+    "bwd": dict(name="bf16 bwd B=1 H=16 N=16384 d=128 non-causal", B=1, H=16, N=16384, d=128, causal=False,
+                window=0, dtype="bf16", direction="bwd"),
+    "bwd_c2": dict(name="bf16 bwd B=2 H=32 N=4096 d=128 causal", B=2, H=32, N=4096, d=128, causal=True, window=0,
+                   dtype="bf16", direction="bwd"),
 }
 
 
@@ -56,6 +64,12 @@ def workload(spec: str) -> dict:
         n, d, c = int(n), int(d), c in ("1", "true", "causal")
         return dict(name=f"bf16 fwd sweep point N={n} d={d} {'causal' if c else 'non-causal'} (16384 tokens, "
                          f"hidden 2048)", B=16384 // n, H=2048 // d, N=n, d=d, causal=c, window=0, dtype="bf16")
+    if spec.startswith("bwd:"):
+        _, n, c = spec.split(":")
+        n, c = int(n), c in ("1", "true", "causal")
+        return dict(name=f"bf16 bwd sweep point N={n} d=128 {'causal' if c else 'non-causal'} (16384 tokens, "
+                         f"hidden 2048)", B=16384 // n, H=16, N=n, d=128, causal=c, window=0, dtype="bf16",
+                    direction="bwd")
     raise SystemExit(f"unknown workload {spec}")
 
 
@@ -68,11 +82,14 @@ def attended_pairs(N: int, causal: bool, window: int) -> int:
 
 
 def flops_per_step(w: dict) -> float:
-    """4 B H N^2 d, halved when causal; with a window, the attended pairs."""
+    """Forward: 4 B H N^2 d, halved when causal; with a window, 4 d x the
+    attended pairs.  Backward: 2.5 x the forward (five matrix products
+    against two, the pages' convention)."""
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    mult = 2.5 if w.get("direction") == "bwd" else 1.0
     if w["window"] > 0:
-        return 4.0 * B * H * d * attended_pairs(N, w["causal"], w["window"])
-    return 4.0 * B * H * N * N * d / (2.0 if w["causal"] else 1.0)
+        return mult * 4.0 * B * H * d * attended_pairs(N, w["causal"], w["window"])
+    return mult * 4.0 * B * H * N * N * d / (2.0 if w["causal"] else 1.0)
 
 
 def load_peaks():
@@ -102,6 +119,7 @@ KERNEL_SOURCES = {
     "attn_fwd": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_bf16_d128.cu"),
     "attn_fwd_fp8": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d128.cu"),
     "fp8_prep": ("fp8_prep.cu", "fp8_prep.cuh"),
+    "attn_bwd": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_bwd_kernel.cuh", "attn_bwd.cu", "attn_bwd.cuh"),
 }
 
 
@@ -207,7 +225,12 @@ def make_inputs(w, device, seed=0):
     arrs = (synth.tensor_bf16((B, N, H, d), seed, synth.STREAM_Q, outliers),
             synth.tensor_bf16((B, N, Hkv, d), seed, synth.STREAM_K, outliers),
             synth.tensor_bf16((B, N, Hkv, d), seed, synth.STREAM_V, outliers))
+    if w.get("direction") == "bwd":
+        arrs = arrs + (synth.tensor_bf16((B, N, H, d), seed, STREAM_DOUT),)
     return [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device) for a in arrs], arrs
+
+
+STREAM_DOUT = 4    # synth stream of the upstream gradient dO
 
 
 def time_loop(fn, steps, stream):
@@ -222,12 +245,7 @@ def time_loop(fn, steps, stream):
     return e0.elapsed_time(e1)
 
 
-def cpu_baseline(w, budget_s=12.0, arrs=None):
-    """The fp64 oracle as it stands, on the host cores, on a bounded sample of
-    query rows of the same workload; throughput in the same unit (TFLOPS of
-    attention arithmetic, 4 d per attended pair)."""
-    import oracle
-
+def _oracle_inputs(w, arrs=None):
     from exact_attention_71_gb300 import synth
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     if arrs is None:
@@ -236,44 +254,85 @@ def cpu_baseline(w, budget_s=12.0, arrs=None):
         arrs = (synth.tensor_bf16((B, N, H, d), 0, synth.STREAM_Q, o_),
                 synth.tensor_bf16((B, N, Hkv, d), 0, synth.STREAM_K, o_),
                 synth.tensor_bf16((B, N, Hkv, d), 0, synth.STREAM_V, o_))
-    q, k, v = arrs
-    cores = os.cpu_count() or 1
+        if w.get("direction") == "bwd":
+            arrs = arrs + (synth.tensor_bf16((B, N, H, d), 0, STREAM_DOUT),)
+    return arrs
 
-    def pairs_of(rows):
-        rows = np.asarray(rows, dtype=np.int64)
-        hi = rows if w["causal"] else np.full(len(rows), N - 1)
-        lo = np.maximum(0, rows - w["window"] + 1) if w["window"] > 0 else np.zeros(len(rows), dtype=np.int64)
-        return int(np.sum(hi - lo + 1)) * B * H
 
-    nrows = 2
-    t = 0.0
-    while True:
-        rows = synth.sample_rows(N, nrows, seed=17)
-        t0 = time.perf_counter()
-        oracle.attention(q, k, v, causal=w["causal"], window=w["window"], rows=rows, nthreads=cores)
+def _oracle_run(w, arrs, size, cores):
+    """One bounded sample of the workload on the fp64 oracle: `size` seeded
+    query rows of every head (forward), or the first `size` query heads in
+    full (backward, whose key gradients need every query row).  Returns
+    (seconds, flops, description)."""
+    import oracle
+
+    from exact_attention_71_gb300 import synth
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    t0 = time.perf_counter()
+    if w.get("direction") == "bwd":
+        q, k, v, do = arrs
+        group = H // k.shape[2]
+        nh = max(group, size // group * group)
+        sl, skv = slice(0, nh), slice(0, nh // group)
+        oracle.attention_bwd(q[:, :, sl], k[:, :, skv], v[:, :, skv], do[:, :, sl], causal=w["causal"],
+                             window=w["window"], nthreads=cores)
         t = time.perf_counter() - t0
-        if t >= budget_s / 2 or nrows >= N:
-            break
-        nrows = min(N, int(nrows * max(1.5, min(8.0, 0.6 * budget_s / max(t, 1e-3)))))
-    flops = 4.0 * d * pairs_of(rows)
+        flops = flops_per_step(dict(w, H=nh))
+        return t, flops, f"{nh} of {H} query heads in full x {B} batch ({flops / 1e9:.2f} GFLOP, fp64, {cores} threads)"
+    q, k, v = arrs[:3]
+    rows = synth.sample_rows(N, size, seed=17)
+    oracle.attention(q, k, v, causal=w["causal"], window=w["window"], rows=rows, nthreads=cores)
+    t = time.perf_counter() - t0
+    rows = np.asarray(rows, dtype=np.int64)
+    hi = rows if w["causal"] else np.full(len(rows), N - 1)
+    lo = np.maximum(0, rows - w["window"] + 1) if w["window"] > 0 else np.zeros(len(rows), dtype=np.int64)
+    flops = 4.0 * d * int(np.sum(hi - lo + 1)) * B * H
+    return t, flops, f"{len(rows)} seeded query rows per head x all {B * H} heads ({flops / 1e9:.2f} GFLOP, fp64, {cores} threads)"
+
+
+def _oracle_size(w, arrs, target_s, cores):
+    """Grows the sample until one run takes at least target_s / 2."""
+    size = 1 if w.get("direction") == "bwd" else 2
+    limit = w["H"] if w.get("direction") == "bwd" else w["N"]
+    while True:
+        t, flops, desc = _oracle_run(w, arrs, size, cores)
+        if t >= target_s / 2 or size >= limit:
+            return size, t, flops, desc
+        size = min(limit, int(size * max(1.5, min(8.0, 0.6 * target_s / max(t, 1e-3)))) + 1)
+
+
+def cpu_baseline(w, budget_s=12.0, arrs=None):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample of
+    the same workload; throughput in the same unit (TFLOPS of attention
+    arithmetic)."""
+    arrs = _oracle_inputs(w, arrs)
+    cores = os.cpu_count() or 1
+    _, t, flops, desc = _oracle_size(w, arrs, budget_s, cores)
     return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows)} seeded query rows per head x all {B * H} heads of the workload "
-                      f"({flops / 1e9:.2f} GFLOP in {t:.1f} s, fp64, {cores} threads)"}
+            "sample": desc + f", {t:.1f} s"}
 
 
 def run_reference(args, w, key):
+    """The oracle arm: W untimed and K timed steps, each the same bounded
+    sample of the workload (sized once so that the whole run stays within
+    about two minutes of CPU time); value = the median step's throughput."""
     ws, rank, _ = dist_setup()
     if rank != 0:
         return
-    per = []
-    cb = None
+    cores = os.cpu_count() or 1
+    arrs = _oracle_inputs(w)
+    per_step = min(args.ref_budget, max(0.05, 120.0 / (args.steps + args.warmup)))
+    size, _, _, _ = _oracle_size(w, arrs, per_step, cores)
     for _ in range(args.warmup):
-        pass
+        _oracle_run(w, arrs, size, cores)
+    per = []
+    desc = ""
     for _ in range(max(1, args.steps)):
-        cb = cpu_baseline(w, budget_s=args.ref_budget)
-        per.append(cb["value"])
+        t, flops, desc = _oracle_run(w, arrs, size, cores)
+        per.append(flops / t / 1e12)
     val = float(np.median(per))
-    cb["value"] = val
+    cb = {"value": val, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+          "sample": desc + f"; median of {len(per)} timed steps"}
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w["name"], "B": w["B"], "H": w["H"], "N": w["N"],
@@ -379,20 +438,29 @@ def main():
     w = dict(w, B=b_stop - b_start)
     # Two resident input sets (> L2 each) used alternately, so no step finds
     # the previous step's inputs in the 129 MB L2.
+    bwd = w.get("direction") == "bwd"
     sets = []
     arrs0 = None
     for s in range(2):
-        (q, k, v), arrs = make_inputs(w, device, seed=s + 2 * b_start)
+        tensors, arrs = make_inputs(w, device, seed=s + 2 * b_start)
         if s == 0:
             arrs0 = arrs
+        q, k, v = tensors[:3]
         if w["dtype"] == "fp8":
             q8, k8, v8, qs, ks, vs = api.fp8_prepare_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, sign_seed=1234)
             sets.append((q8, k8, v8, qs, ks, vs))
+        elif bwd:
+            # The backward consumes the forward's O and LSE, computed once here.
+            o_s, lse_s = api.attn_fwd(q, k, v, causal=w["causal"], window=w["window"])
+            sets.append((tensors[3], q, k, v, o_s, lse_s))
         else:
             sets.append((q, k, v))
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=device)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    if bwd:
+        grads = (torch.empty_like(sets[0][1]), torch.empty_like(sets[0][2]), torch.empty_like(sets[0][3]))
+        work = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=device)
     step_idx = [0]
 
     def step():
@@ -400,6 +468,9 @@ def main():
         step_idx[0] += 1
         if w["dtype"] == "fp8":
             api.attn_fwd_fp8(*s, causal=w["causal"], window=w["window"], out=o, lse=lse, stream=stream)
+        elif bwd:
+            api.attn_bwd(*s, causal=w["causal"], window=w["window"], dq=grads[0], dk=grads[1], dv=grads[2],
+                         workspace=work, stream=stream)
         else:
             api.attn_fwd(*s, causal=w["causal"], window=w["window"], out=o, lse=lse, stream=stream)
 
@@ -428,7 +499,7 @@ def main():
     value = ws * flops * args.steps / (ms_total / 1e3) / 1e12
     peaks, peak_src = load_peaks()
     achieved = flops / (ms_step / 1e3) / 1e12
-    kernel = "attn_fwd_fp8" if w["dtype"] == "fp8" else "attn_fwd"
+    kernel = "attn_fwd_fp8" if w["dtype"] == "fp8" else ("attn_bwd" if bwd else "attn_fwd")
     if w["dtype"] == "fp8":
         fp8_peak = peaks.get("fp8_tflops") or 2.0 * peaks["bf16_tflops"]
         peak, peak_note = fp8_peak, f"{peak_src} bf16 burst x 2 (nominal fp8:bf16 ratio)"
@@ -451,12 +522,17 @@ def main():
                        "l2": "inputs larger than L2 (two resident input sets, alternated per step)",
                        "global_batch": global_batch,
                        "parallelism": f"batch shards x{ws}, no collective on the data path"},
-            "roofline": roof, "gpu_launches": args.steps, "clocks": clk.summary() if rank == 0 else None}
+            "roofline": roof, "gpu_launches": args.steps * (3 if bwd else 1),
+            "clocks": clk.summary() if rank == 0 else None}
+    if bwd:
+        line["roofline"]["note"] = ("achieved counts the whole backward step: the fused kernel plus the two "
+                                    "memory-bound launches around it (D / accumulator zeroing, dQ conversion)")
 
     if not args.quick and rank == 0:
         line["e2e"] = e2e_measure(api, w, device, stream, arrs0, flops, steps=min(args.steps, 20))
         if w["dtype"] == "bf16" and args.workload == "c2":
             line["fp8"] = fp8_secondary(api, device, stream, steps=min(args.steps, 200))
+            line["bwd"] = bwd_secondary(api, device, stream, steps=min(args.steps, 50))
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.ref_budget, arrs=arrs0)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -469,6 +545,8 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
     Q, K, V copied to the device, the forward, O and LSE copied back, all
     inside the timed region."""
     import torch
+    if w.get("direction") == "bwd":
+        return e2e_measure_bwd(api, w, device, stream, arrs, flops, steps)
     hq, hk, hv = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in arrs)
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     dq, dk, dv = (torch.empty_like(t, device=device) for t in (hq, hk, hv))
@@ -498,10 +576,72 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
         step()
     torch.cuda.synchronize(device)
     ms = time_loop(step, steps, stream) / steps
-    h2d = 3 * hq.numel() * 2
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
     d2h = ho.numel() * 2 + hl.numel() * 4
     return {"value": round(flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "kernel_launches_per_step": launches}
+
+
+def bwd_secondary(api, device, stream, steps):
+    """The backward on its headline point (the pages' Fig. 6: d=128,
+    non-causal, N=16k, 16 heads), timed like the main line."""
+    import torch
+    w = dict(WORKLOADS["bwd"])
+    tensors, _ = make_inputs(w, device, seed=0)
+    do, (q, k, v) = tensors[3], tensors[:3]
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    o, lse = api.attn_fwd(q, k, v, causal=False)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    work = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=device)
+
+    def fn():
+        api.attn_bwd(do, q, k, v, o, lse, causal=False, dq=dq, dk=dk, dv=dv, workspace=work, stream=stream)
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(device)
+    ms = time_loop(fn, steps, stream) / steps
+    flops = flops_per_step(w)
+    peaks, src = load_peaks()
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": w["name"], "flops_per_step": flops, "ms": round(ms, 4), "tflops": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "launches_per_step": 3,
+            "flop_convention": "2.5 x the forward's 4 B H N^2 d (five products against two)"}
+
+
+def e2e_measure_bwd(api, w, device, stream, arrs, flops, steps):
+    """Backward end to end with HOST buffers: pinned Q, K, V, dO and the
+    forward's O, LSE copied in, attn_bwd, dQ, dK, dV copied back, all inside
+    the timed region."""
+    import torch
+    host = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in arrs]
+    hq, hk, hv, hdo = host
+    dq_, dk_, dv_, ddo = (torch.empty_like(t, device=device) for t in host)
+    o_dev, lse_dev = api.attn_fwd(dq_.copy_(hq), dk_.copy_(hk), dv_.copy_(hv), causal=w["causal"], window=w["window"])
+    ho, hl = o_dev.cpu().pin_memory(), lse_dev.cpu().pin_memory()
+    do_dev, dl_dev = torch.empty_like(o_dev), torch.empty_like(lse_dev)
+    gq, gk, gv = torch.empty_like(dq_), torch.empty_like(dk_), torch.empty_like(dv_)
+    hgq, hgk, hgv = (torch.empty_like(t, device="cpu").pin_memory() for t in (gq, gk, gv))
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    work = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=device)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for dst, src in ((dq_, hq), (dk_, hk), (dv_, hv), (ddo, hdo), (do_dev, ho), (dl_dev, hl)):
+                dst.copy_(src, non_blocking=True)
+            api.attn_bwd(ddo, dq_, dk_, dv_, do_dev, dl_dev, causal=w["causal"], window=w["window"], dq=gq, dk=gk,
+                         dv=gv, workspace=work, stream=stream)
+            for dst, src in ((hgq, gq), (hgk, gk), (hgv, gv)):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    ms = time_loop(step, steps, stream) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, ho, hl))
+    d2h = sum(t.numel() * t.element_size() for t in (hgq, hgk, hgv))
+    return {"value": round(flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "kernel_launches_per_step": 3}
 
 
 def fp8_secondary(api, device, stream, steps):

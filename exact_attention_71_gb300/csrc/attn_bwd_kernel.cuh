@@ -16,7 +16,7 @@
 //     S^T  = K Q^T      (M = 128 keys,  N = 64 queries, K = d)
 //     dP^T = V dO^T     (M = 128 keys,  N = 64 queries, K = d)
 //     dV  += P^T dO     (A = P^T from tensor memory, B = dO MN-major)
-//     dK  += dS^T Q     (A = dS^T from tensor memory, B = Q MN-major)
+//     dK  += dS^T Q     (A = dS^T from shared memory, B = Q MN-major)
 //     dQ^T = K^T dS^T   (A = K read MN-major, B = dS^T from shared memory)
 // and dQ^T (128 dims x 64 queries) is added into a float32 accumulator in
 // global memory with one bulk reduction per step (other key tiles add into
@@ -31,8 +31,12 @@
 //   warp  9    MMA issuer (one elected lane)
 // Tensor memory (512 columns): dV [0, d), dK [d, 2d), S^T double-buffered
 // at 2d and 2d + 64, dP^T at 2d + 128, dQ^T at 2d + 192.  P (bf16 pairs)
-// overwrites the first 32 columns of its S^T buffer and dS the first 32 of
-// dP^T.
+// overwrites the first 32 columns of its S^T buffer.  dS^T goes to shared
+// memory only (double-buffered), where it serves as the K-major A operand of
+// dK and the MN-major B operand of dQ^T; so dP^T of the next step can be
+// issued as soon as this step's dS is written, ahead of dK and dQ^T, and the
+// elementwise warps compute the next dS while the pipe runs them.
+// Issue order of step t: dV(t), S(t+1), dP(t+1), dK(t), dQ^T(t).
 //
 // Every barrier wait is bounded (the forward kernel's failure protocol):
 // a role that gives up records a site code, raises the shared abort flag and
@@ -90,20 +94,22 @@ struct BwdCfg {
     static constexpr int KV_TILE = BN * D * 2;
     static constexpr int NST = 2;                         // Q / dO ring depth
     static constexpr int STAGE = 2 * Q_TILE;              // Q, dO
-    static constexpr int DS_BYTES = BN * BM * 2;          // dS^T, one 128-byte row per key
+    static constexpr int DS_BYTES = BN * BM * 2;          // dS^T, one 128-byte row per key (x2 buffers)
     static constexpr int DQ_STAGE = BM * D * 4;           // float32 dQ tile
     static constexpr int VEC_BYTES = 2 * BM * 4;          // LSE2 and D of one step
     static constexpr int DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + 2 * BM, DQ_COL = 2 * D + 3 * BM;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int EW_WARP0 = 0, DQ_WARP0 = 4, LOAD_WARP = 8, MMA_WARP = 9;
-    static constexpr int THREADS = 320;
+    // Two elementwise warpgroups, each owning 32 of the 64 query columns.
+    static constexpr int EW_WGS = 2, EW_COLS = BM / EW_WGS;
+    static constexpr int EW_WARP0 = 0, DQ_WARP0 = 4 * EW_WGS, LOAD_WARP = DQ_WARP0 + 4, MMA_WARP = LOAD_WARP + 1;
+    static constexpr int THREADS = (MMA_WARP + 1) * 32;
     static constexpr int BAR_BYTES = 256;
     // Shared memory (offsets from a 1024-byte aligned base).
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + KV_TILE;
     static constexpr int OFF_STAGE = OFF_V + KV_TILE;
     static constexpr int OFF_DS = OFF_STAGE + NST * STAGE;
-    static constexpr int OFF_DQ = OFF_DS + DS_BYTES;
+    static constexpr int OFF_DQ = OFF_DS + 2 * DS_BYTES;
     static constexpr int OFF_VEC = OFF_DQ + 2 * DQ_STAGE;
     static constexpr int OFF_BAR = OFF_VEC + NST * VEC_BYTES;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
@@ -168,14 +174,26 @@ struct BwdItem {
     int b, hk, k0;           // batch, key/value head, first key
     int i_lo, n_i;           // query tiles [i_lo, i_lo + n_i)
     int steps;               // group * n_i
+    int rot;                 // first query tile offset (spreads the dQ adds)
+    // Query head and first query row of step t.  The CTAs of one head start
+    // their walk over the query tiles at different tiles, so that their bulk
+    // adds into the float32 dQ accumulator do not all hit the same rows.
+    __device__ __forceinline__ int head(int t, int group) const { return hk * group + t / n_i; }
+    __device__ __forceinline__ int q0(int t, int bm) const {
+        int i = t % n_i + rot;
+        if (i >= n_i) i -= n_i;
+        return (i_lo + i) * bm;
+    }
 };
 
 template <class Cfg>
 __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p) {
     BwdItem w;
-    const int bhk_count = p.B * p.H_kv;
-    const int kb = static_cast<int>(blockIdx.x) / bhk_count;     // heaviest (first) key tiles first
-    const int bhk = static_cast<int>(blockIdx.x) % bhk_count;
+    // Head-major order: the CTAs running together share a few heads, so the
+    // heads' Q, dO and float32 dQ accumulators stay in L2 while every key
+    // tile of the head walks them.
+    const int kb = static_cast<int>(blockIdx.x) % p.n_kblocks;
+    const int bhk = static_cast<int>(blockIdx.x) / p.n_kblocks;
     w.b = bhk / p.H_kv;
     w.hk = bhk % p.H_kv;
     w.k0 = kb * Cfg::BN;
@@ -187,6 +205,9 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdParams& p) {
     w.i_lo = lo;
     w.n_i = hi >= lo ? hi - lo + 1 : 0;
     w.steps = w.n_i * p.group;
+    // Key tile kb starts at query tile kb * BN / BM of its range: at any
+    // moment the CTAs of one head are on different query tiles.
+    w.rot = w.n_i > 0 ? static_cast<int>((static_cast<long long>(kb) * (Cfg::BN / Cfg::BM)) % w.n_i) : 0;
     return w;
 }
 
@@ -216,12 +237,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         mbar_init(&bars->kv_full, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->q_full[s], 1);
-            mbar_init(&bars->q_empty[s], 1 + 4);    // the MMAs' commit + the four elementwise warps
+            mbar_init(&bars->q_empty[s], 1 + 4 * Cfg::EW_WGS);   // the MMAs' commit + every elementwise warp
             mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->p_full[s], 128);
+            mbar_init(&bars->p_full[s], 128 * Cfg::EW_WGS);
         }
         mbar_init(&bars->dp_full, 1);
-        mbar_init(&bars->ds_full, 128);
+        mbar_init(&bars->ds_full, 128 * Cfg::EW_WGS);
         mbar_init(&bars->dq_full, 1);
         mbar_init(&bars->dq_empty, 128);
         mbar_init(&bars->acc_full, 1);
@@ -261,8 +282,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (; t < T; ++t) {
                 const int st = t % NST;
                 if (!bwait(&bars->q_empty[st], ((t / NST) & 1) ^ 1, abort_flag, p, BSITE_LOAD_EMPTY)) break;
-                const int h = w.hk * p.group + t / w.n_i;
-                const int q0 = (w.i_lo + t % w.n_i) * BM;
+                const int h = w.head(t, p.group);
+                const int q0 = w.q0(t, BM);
                 uint8_t* dst = sStage + st * Cfg::STAGE;
                 mbar_arrive_expect_tx(&bars->q_full[st], Cfg::STAGE + Cfg::VEC_BYTES);
 #pragma unroll
@@ -288,9 +309,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint64_t k_kmaj = sdesc_sw128(aK, 16, 1024);
             const uint64_t v_kmaj = sdesc_sw128(aV, 16, 1024);
             const uint64_t k_mn = sdesc_sw128(aK, BN * 128, 1024);          // K^T as the A operand of dQ^T
-            const uint64_t ds_mn = sdesc_sw128(aDS, BN * 128, 1024);        // dS^T as the B operand of dQ^T
+
             constexpr uint32_t id_s = make_idesc_ab(1, 128, BM, 0, 0);      // S^T, dP^T
             constexpr uint32_t id_acc = make_idesc_ab(1, 128, D, 0, 1);     // dV, dK (B MN-major)
+            // dS^T buffer of step t: rows = keys, 64 queries (128 bytes) each.
+            auto ds_addr = [&](int t) { return aDS + (t & 1) * Cfg::DS_BYTES; };
             constexpr uint32_t id_dq = make_idesc_ab(1, D, BM, 1, 1);       // dQ^T (A, B MN-major)
             bool ok = bwait_warp(&bars->kv_full, 0, abort_flag, p, BSITE_MMA_KV);
 
@@ -307,12 +330,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             };
             // acc (+)= X^T Y with X^T (bf16 pairs) in tensor memory at x_col and
             // Y (64 query rows x d) in shared memory, read MN-major.
+            // P^T of query columns [32 g, 32 g + 32) sits at columns
+            // [32 g, 32 g + 16) of its S^T buffer (written by warpgroup g).
             auto issue_acc = [&](uint32_t d_col, uint32_t x_col, uint32_t y_addr, bool accumulate) {
                 const uint64_t y_desc = sdesc_sw128(y_addr, BM * 128, 1024);
 #pragma unroll
-                for (int kk = 0; kk < BM / 16; ++kk)
-                    mma_f16_ts(tmem + d_col, tmem + x_col + kk * 8, y_desc + ((kk * 16 * 128) >> 4), id_acc,
+                for (int kk = 0; kk < BM / 16; ++kk) {
+                    constexpr int per_wg = Cfg::EW_COLS / 16;
+                    const uint32_t a_col = x_col + (kk / per_wg) * Cfg::EW_COLS + (kk % per_wg) * 8;
+                    mma_f16_ts(tmem + d_col, tmem + a_col, y_desc + ((kk * 16 * 128) >> 4), id_acc,
                                (accumulate || kk > 0) ? 1u : 0u);
+                }
             };
             auto stage_addr = [&](int t) { return smem_u32(sStage + (t % NST) * Cfg::STAGE); };
 
@@ -348,14 +376,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     __syncwarp();
                 }
-                // dK += dS^T Q, then dQ^T = K^T dS^T
+                // dS(t) is in shared memory and dP^T(t) has been read: dP^T of
+                // the next step first, then dK += dS^T Q and dQ^T = K^T dS^T.
                 if (!bwait_warp(&bars->ds_full, t & 1, abort_flag, p, BSITE_MMA_DS)) { ok = false; break; }
                 tc_fence_after();
-                if (elect_one()) issue_acc(Cfg::DK_COL, Cfg::DP_COL, sa, t > 0);
+                if (elect_one()) {
+                    if (t + 1 < T) {
+                        issue_kq(Cfg::DP_COL, v_kmaj, stage_addr(t + 1) + Cfg::Q_TILE);
+                        mma_commit(&bars->dp_full);
+                    }
+                    const uint64_t ds_k = sdesc_sw128(ds_addr(t), 16, 1024);
+                    const uint64_t q_mn = sdesc_sw128(sa, BM * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BM / 16; ++kk)
+                        mma_f16_ss(tmem + Cfg::DK_COL, ds_k + ((kk * 32) >> 4), q_mn + ((kk * 16 * 128) >> 4), id_acc,
+                                   (t > 0 || kk > 0) ? 1u : 0u);
+                }
                 __syncwarp();
                 if (!bwait_warp(&bars->dq_empty, (t & 1) ^ 1, abort_flag, p, BSITE_MMA_DQ)) { ok = false; break; }
                 tc_fence_after();
                 if (elect_one()) {
+                    const uint64_t ds_mn = sdesc_sw128(ds_addr(t), BN * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
                         mma_f16_ss(tmem + Cfg::DQ_COL, k_mn + ((kk * 16 * 128) >> 4), ds_mn + ((kk * 16 * 128) >> 4),
@@ -363,12 +404,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     mma_commit(&bars->dq_full);
                     // Q_t and dO_t are no longer read by any MMA.
                     mma_commit(&bars->q_empty[t % NST]);
-                    if (t + 1 < T) {
-                        issue_kq(Cfg::DP_COL, v_kmaj, stage_addr(t + 1) + Cfg::Q_TILE);
-                        mma_commit(&bars->dp_full);
-                    } else {
-                        mma_commit(&bars->acc_full);
-                    }
+                    if (t + 1 == T) mma_commit(&bars->acc_full);
                 }
                 __syncwarp();
             }
@@ -381,6 +417,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
     } else if (warp < Cfg::DQ_WARP0) {
         // ------------------------------------------------------------ elementwise: P, dS
+        constexpr int EC = Cfg::EW_COLS;                 // query columns of this warpgroup
+        const int g = warp >> 2;                         // warpgroup: columns [g EC, g EC + EC)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                  // key row of the tile
         const int key = w.k0 + r;
@@ -388,40 +426,41 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         bool ok = true;
         for (int t = 0; t < T && ok; ++t) {
             const int st = t % NST;
-            const int q0 = (w.i_lo + t % w.n_i) * BM;
-            const uint32_t s_tm = tmem + lane_off + Cfg::S_COL + (t & 1) * BM;
-            const uint32_t dp_tm = tmem + lane_off + Cfg::DP_COL;
+            const int q0 = w.q0(t, BM) + g * EC;
+            const uint32_t s_tm = tmem + lane_off + Cfg::S_COL + (t & 1) * BM + g * EC;
+            const uint32_t dp_tm = tmem + lane_off + Cfg::DP_COL + g * EC;
             if (!bwait_warp(&bars->q_full[st], (t / NST) & 1, abort_flag, p, BSITE_EW_Q)) { ok = false; break; }
             if (!bwait_warp(&bars->s_full[t & 1], (t >> 1) & 1, abort_flag, p, BSITE_EW_S)) { ok = false; break; }
             tc_fence_after();
-            const float* lse2 = sVec + st * (2 * BM);
+            const float* lse2 = sVec + st * (2 * BM) + g * EC;
             const float* dvec = lse2 + BM;
             // Visible queries of this key: [qlo, qhi].
             const int qlo = p.causal ? key : 0;
             const int qhi = p.window > 0 ? key + p.window - 1 : 0x7fffffff;
             const bool key_ok = key < p.N;
-            const bool full = key_ok && q0 >= qlo && q0 + BM - 1 <= qhi;
-            float pr[BM];
-#pragma unroll
-            for (int c = 0; c < BM / 32; ++c) {
-                uint32_t sr[32];
-                tmem_ld32(s_tm + c * 32, sr);
+            const bool full = key_ok && q0 >= qlo && q0 + EC - 1 <= qhi;
+            float pr[EC];
+            {
+                uint32_t sr[EC];
+                tmem_ld32(s_tm, sr);
                 tmem_wait_ld();
                 reg_fence32(sr);
-                uint32_t pk[16];
+                uint32_t pk[EC / 2];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int qi = c * 32 + x;
-                    float v = ex2_approx(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[qi]));
+                for (int x = 0; x < EC; ++x) {
+                    float v = ex2_approx(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[x]));
                     if (!full) {
-                        const int q = q0 + qi;
+                        const int q = q0 + x;
                         if (!key_ok || q < qlo || q > qhi) v = 0.0f;
                     }
-                    pr[qi] = v;
+                    pr[x] = v;
                 }
 #pragma unroll
-                for (int x = 0; x < 16; ++x) pk[x] = pack_bf16x2(pr[c * 32 + 2 * x], pr[c * 32 + 2 * x + 1]);
-                tmem_st16(s_tm + c * 16, pk);
+                for (int x = 0; x < EC / 2; ++x) pk[x] = pack_bf16x2(pr[2 * x], pr[2 * x + 1]);
+                // P^T over the first half of this warpgroup's own S^T columns
+                // (read above), so the two warpgroups never overwrite each
+                // other's scores.
+                tmem_st16(s_tm, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -429,32 +468,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
             if (!bwait_warp(&bars->dp_full, t & 1, abort_flag, p, BSITE_EW_DP)) { ok = false; break; }
             tc_fence_after();
-            uint8_t* ds_row = sDS + r * 128;
-#pragma unroll
-            for (int c = 0; c < BM / 32; ++c) {
-                uint32_t dr[32];
-                tmem_ld32(dp_tm + c * 32, dr);
+            // dS^T(t) goes to buffer t & 1; the MMAs of step t - 2 that read
+            // it were issued before dP^T(t), whose completion this thread has
+            // just observed.
+            uint8_t* ds_row = sDS + (t & 1) * Cfg::DS_BYTES + r * 128;
+            {
+                uint32_t dr[EC];
+                tmem_ld32(dp_tm, dr);
                 tmem_wait_ld();
                 reg_fence32(dr);
-                uint32_t pk[16];
+                uint32_t pk[EC / 2];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int qi = c * 32 + 2 * x;
-                    const float d0 = pr[qi] * (__uint_as_float(dr[2 * x]) - dvec[qi]);
-                    const float d1 = pr[qi + 1] * (__uint_as_float(dr[2 * x + 1]) - dvec[qi + 1]);
+                for (int x = 0; x < EC / 2; ++x) {
+                    const float d0 = pr[2 * x] * (__uint_as_float(dr[2 * x]) - dvec[2 * x]);
+                    const float d1 = pr[2 * x + 1] * (__uint_as_float(dr[2 * x + 1]) - dvec[2 * x + 1]);
                     pk[x] = pack_bf16x2(d0, d1);
                 }
-                tmem_st16(dp_tm + c * 16, pk);
                 // dS^T row of this key into shared memory (128-byte swizzle:
-                // 16-byte chunk j of row r sits at chunk j ^ (r % 8)).
+                // 16-byte chunk j of row r sits at chunk j ^ (r % 8)); this
+                // warpgroup owns chunks [4 g, 4 g + 4).
 #pragma unroll
                 for (int y = 0; y < 4; ++y) {
-                    const int chunk = (c * 4 + y) ^ (r & 7);
+                    const int chunk = (g * 4 + y) ^ (r & 7);
                     *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
                         make_uint4(pk[4 * y], pk[4 * y + 1], pk[4 * y + 2], pk[4 * y + 3]);
                 }
             }
-            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bars->ds_full);
@@ -462,31 +501,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->q_empty[st]);
         }
-        // dV epilogue: thread = key row.
-        if (ok && T > 0) ok = bwait_warp(&bars->acc_full, 0, abort_flag, p, BSITE_EW_ACC);
-        if (ok || T == 0) {
-            tc_fence_after();
-            const bool store = key < p.N;
-            __nv_bfloat16* row =
-                reinterpret_cast<__nv_bfloat16*>(p.dv) + ((static_cast<size_t>(w.b) * p.N + key) * p.H_kv + w.hk) * D;
+        // dV epilogue (warpgroup 0): thread = key row.
+        if (g == 0) {
+            if (ok && T > 0) ok = bwait_warp(&bars->acc_full, 0, abort_flag, p, BSITE_EW_ACC);
+            if (ok || T == 0) {
+                tc_fence_after();
+                const bool store = key < p.N;
+                __nv_bfloat16* row =
+                    reinterpret_cast<__nv_bfloat16*>(p.dv) + ((static_cast<size_t>(w.b) * p.N + key) * p.H_kv + w.hk) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32];
-                if (T > 0) {
-                    tmem_ld32(tmem + lane_off + Cfg::DV_COL + c * 32, a);
-                    tmem_wait_ld();
-                    reg_fence32(a);
-                } else {
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t a[32];
+                    if (T > 0) {
+                        tmem_ld32(tmem + lane_off + Cfg::DV_COL + c * 32, a);
+                        tmem_wait_ld();
+                        reg_fence32(a);
+                    } else {
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) a[x] = 0u;
-                }
-                uint32_t pk[16];
+                        for (int x = 0; x < 32; ++x) a[x] = 0u;
+                    }
+                    uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) pk[x] = pack_bf16x2(__uint_as_float(a[2 * x]), __uint_as_float(a[2 * x + 1]));
-                if (store) {
-                    uint4* dst = reinterpret_cast<uint4*>(row + c * 32);
+                    for (int x = 0; x < 16; ++x) pk[x] = pack_bf16x2(__uint_as_float(a[2 * x]), __uint_as_float(a[2 * x + 1]));
+                    if (store) {
+                        uint4* dst = reinterpret_cast<uint4*>(row + c * 32);
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+                        for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+                    }
                 }
             }
         }
@@ -498,8 +539,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const bool leader = threadIdx.x == Cfg::DQ_WARP0 * 32;
         bool ok = true;
         for (int t = 0; t < T && ok; ++t) {
-            const int h = w.hk * p.group + t / w.n_i;
-            const int q0 = (w.i_lo + t % w.n_i) * BM;
+            const int h = w.head(t, p.group);
+            const int q0 = w.q0(t, BM);
             if (!bwait_warp(&bars->dq_full, t & 1, abort_flag, p, BSITE_DQ_FULL)) { ok = false; break; }
             tc_fence_after();
             uint32_t a[BM];
