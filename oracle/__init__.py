@@ -44,6 +44,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_attn_fwd_bf16.restype = i
             L.oracle_attn_fwd_f64.argtypes = [P, P, P, P, P, i, i, i, i, i, i, d, i, P, i, i]
             L.oracle_attn_fwd_f64.restype = i
+            L.oracle_attn_fwd_bf16_masked.argtypes = [P, P, P, P, P, i, i, i, i, i, i, d, i, P, P, i, i]
+            L.oracle_attn_fwd_bf16_masked.restype = i
+            L.oracle_attn_fwd_f64_masked.argtypes = [P, P, P, P, P, i, i, i, i, i, i, d, i, P, P, i, i]
+            L.oracle_attn_fwd_f64_masked.restype = i
             L.oracle_attn_bwd_bf16.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, d, i, i]
             L.oracle_attn_bwd_bf16.restype = i
             L.oracle_attn_bwd_f64.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, d, i, i]
@@ -79,8 +83,12 @@ def _rows_arg(rows, N):
     return r, len(r), _ptr(r)
 
 
-def attention(q, k, v, causal=False, scale=None, window=0, rows=None, nthreads=0):
+def attention(q, k, v, causal=False, scale=None, window=0, rows=None, nthreads=0, block_mask=None):
     """Attention forward in fp64.
+
+    block_mask: optional uint8 (B, H, T, T), T = ceil(N / 128): query block i
+    sees key block j of (b, h) iff block_mask[b, h, i, j] != 0 (ANDed with the
+    causal and window masks).
 
     q: (B, N, H, d); k, v: (B, N, Hkv, d) with Hkv dividing H (grouped-query
     attention: query head h reads key/value head h // (H // Hkv)).  Arrays are
@@ -95,14 +103,23 @@ def attention(q, k, v, causal=False, scale=None, window=0, rows=None, nthreads=0
     rr, R, rp = _rows_arg(rows, N)
     o = np.empty((B, H, R, d), dtype=np.float64)
     lse = np.empty((B, H, R), dtype=np.float64)
-    if q.dtype == np.uint16:
-        fn = lib().oracle_attn_fwd_bf16
+    bf16 = q.dtype == np.uint16
+    if bf16:
         q, k, v = (np.ascontiguousarray(t, dtype=np.uint16) for t in (q, k, v))
     else:
-        fn = lib().oracle_attn_fwd_f64
         q, k, v = (np.ascontiguousarray(t, dtype=np.float64) for t in (q, k, v))
-    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d, int(bool(causal)),
-            float(scale), int(window), rp, R, int(nthreads))
+    if block_mask is None:
+        fn = lib().oracle_attn_fwd_bf16 if bf16 else lib().oracle_attn_fwd_f64
+        rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d, int(bool(causal)),
+                float(scale), int(window), rp, R, int(nthreads))
+    else:
+        T = (N + 127) // 128
+        m = np.ascontiguousarray(block_mask, dtype=np.uint8)
+        if m.shape != (B, H, T, T):
+            raise ValueError(f"block_mask must be (B, H, {T}, {T})")
+        fn = lib().oracle_attn_fwd_bf16_masked if bf16 else lib().oracle_attn_fwd_f64_masked
+        rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d, int(bool(causal)),
+                float(scale), int(window), _ptr(m), rp, R, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_attn_fwd: bad arguments")
     return o, lse

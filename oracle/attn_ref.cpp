@@ -24,7 +24,10 @@
 //     O_i   = sum_j exp(s_j - m) v_j / l
 //     LSE_i = m + log(l)                        (natural log)
 // Visibility of key j to query i: j <= i when causal; j > i - window when
-// window > 0.  A row that sees no key gets O = 0 and LSE = -inf.
+// window > 0; and, with a block-sparse mask (the practitioner's FA3 post,
+// §3.3: the caller decides per query block and key block whether the pair
+// takes part), mask[b][h][i / 128][j / 128] != 0.  A row that sees no key
+// gets O = 0 and LSE = -inf.
 //
 // FP8 prep (block quantization + incoherent processing, [R] §2.2 / §3.3):
 //     r   = x M  with M = D H_d / sqrt(d)   (Q and K; V is not rotated)
@@ -90,7 +93,7 @@ double bf16_value(uint16_t bits) {
     return static_cast<double>(f);
 }
 
-bool key_visible(long i, long j, int causal, int window) {
+bool key_visible_plain(long i, long j, int causal, int window) {
     if (causal && j > i) return false;
     if (window > 0 && j <= i - window) return false;
     return true;
@@ -124,10 +127,16 @@ void parallel_for(long count, int nthreads, F&& body) {
 // One query row of one (batch, head): the plain two-pass definition.
 // in(b, n, h, c) reads element c of token n, head h of batch b from a
 // (B, N, H, d) tensor.  probs (optional) receives the N softmax weights.
+// plane: the (b, h) plane of a block mask, T x T with T = ceil(N / 128), or
+// nullptr for none.
 template <class In>
 void attention_row(const In& qin, const In& kin, const In& vin, long b, long h, long i,
                    long N, long d, int causal, double scale, int window,
-                   double* o_row, double* lse_out, double* probs) {
+                   double* o_row, double* lse_out, double* probs, const uint8_t* plane = nullptr) {
+    const long T = (N + 127) / 128;
+    auto key_visible = [&](long ii, long j, int c, int w) {
+        return key_visible_plain(ii, j, c, w) && (!plane || plane[(ii / 128) * T + j / 128] != 0);
+    };
     std::vector<double> s(N, -std::numeric_limits<double>::infinity());
     std::vector<double> q(d);
     for (long c = 0; c < d; ++c) q[c] = qin(b, i, h, c);
@@ -184,7 +193,7 @@ struct F64Tensor {
 template <class In>
 int run_attention(const In& q, const In& k, const In& v, double* o, double* lse,
                   int B, int H, int N, int d, int causal, double scale, int window,
-                  const int* rows, int nrows, int nthreads) {
+                  const int* rows, int nrows, int nthreads, const uint8_t* block_mask = nullptr) {
     if (B < 0 || H < 0 || N < 0 || d <= 0) return -1;
     const long R = rows ? nrows : N;
     for (long r = 0; rows && r < R; ++r) if (rows[r] < 0 || rows[r] >= N) return -1;
@@ -194,8 +203,10 @@ int run_attention(const In& q, const In& k, const In& v, double* o, double* lse,
         const long bh = it / R;
         const long b = bh / H, h = bh % H;
         const long i = rows ? rows[r] : r;
+        const long T = (static_cast<long>(N) + 127) / 128;
+        const uint8_t* plane = block_mask ? block_mask + (b * H + h) * T * T : nullptr;
         attention_row(q, k, v, b, h, i, N, d, causal, scale, window,
-                      o + it * d, lse + it, nullptr);
+                      o + it * d, lse + it, nullptr, plane);
     });
     return 0;
 }
@@ -281,7 +292,7 @@ void backward_row(const In& qin, const In& kin, const In& vin, const In& doin, l
     for (long c = 0; c < d; ++c) dout[c] = doin(b, i, h, c);
     double D = 0.0;
     for (long j = 0; j < N; ++j) {
-        if (!key_visible(i, j, causal, window)) continue;
+        if (!key_visible_plain(i, j, causal, window)) continue;
         double acc = 0.0;
         for (long c = 0; c < d; ++c) acc += dout[c] * vin(b, j, h, c);
         dp[j] = acc;
@@ -289,7 +300,7 @@ void backward_row(const In& qin, const In& kin, const In& vin, const In& doin, l
     }
     for (long c = 0; c < d; ++c) dq_row[c] = 0.0;
     for (long j = 0; j < N; ++j) {
-        if (!key_visible(i, j, causal, window)) continue;
+        if (!key_visible_plain(i, j, causal, window)) continue;
         const double ds = p[j] * (dp[j] - D);
         for (long c = 0; c < d; ++c) dq_row[c] += ds * kin(b, j, h, c);
     }
@@ -309,7 +320,7 @@ void backward_key(const In& qin, const In& kin, const In& vin, const In& doin, c
         const double* lse_h = lse + (b * H + h) * N;
         const double* D_h = Dv + (b * H + h) * N;
         for (long i = 0; i < N; ++i) {
-            if (!key_visible(i, j, causal, window)) continue;
+            if (!key_visible_plain(i, j, causal, window)) continue;
             double s = 0.0, dp = 0.0;
             for (long c = 0; c < d; ++c) {
                 s += qin(b, i, h, c) * kin(b, j, h, c);
@@ -376,6 +387,25 @@ int oracle_attn_fwd_bf16(const uint16_t* q, const uint16_t* k, const uint16_t* v
     if (Hkv <= 0 || H % Hkv != 0) return -1;
     Bf16Tensor Q{q, N, H, d, 1}, K{k, N, Hkv, d, H / Hkv}, V{v, N, Hkv, d, H / Hkv};
     return run_attention(Q, K, V, o, lse, B, H, N, d, causal, scale, window, rows, nrows, nthreads);
+}
+
+// As oracle_attn_fwd_bf16 with a block mask (B, H, T, T), T = ceil(N / 128).
+int oracle_attn_fwd_bf16_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                double* o, double* lse, int B, int H, int Hkv, int N, int d,
+                                int causal, double scale, int window, const uint8_t* block_mask,
+                                const int* rows, int nrows, int nthreads) {
+    if (Hkv <= 0 || H % Hkv != 0) return -1;
+    Bf16Tensor Q{q, N, H, d, 1}, K{k, N, Hkv, d, H / Hkv}, V{v, N, Hkv, d, H / Hkv};
+    return run_attention(Q, K, V, o, lse, B, H, N, d, causal, scale, window, rows, nrows, nthreads, block_mask);
+}
+
+int oracle_attn_fwd_f64_masked(const double* q, const double* k, const double* v,
+                               double* o, double* lse, int B, int H, int Hkv, int N, int d,
+                               int causal, double scale, int window, const uint8_t* block_mask,
+                               const int* rows, int nrows, int nthreads) {
+    if (Hkv <= 0 || H % Hkv != 0) return -1;
+    F64Tensor Q{q, N, H, d, 1}, K{k, N, Hkv, d, H / Hkv}, V{v, N, Hkv, d, H / Hkv};
+    return run_attention(Q, K, V, o, lse, B, H, N, d, causal, scale, window, rows, nrows, nthreads, block_mask);
 }
 
 int oracle_attn_fwd_f64(const double* q, const double* k, const double* v,
