@@ -55,6 +55,8 @@ def library() -> ctypes.CDLL:
         L.attn_fp8_prep_rope.argtypes = [P, P, P, P, P, i, i, i, i, i, i, u64, i, P]
         L.attn_fp8_prep_rope.restype = i
         L.attn_fp8_prep.restype = i
+        L.attn_fwd_sparse.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, f, i, P]
+        L.attn_fwd_sparse.restype = i
         sz = ctypes.c_size_t
         L.attn_bwd_workspace_size.argtypes = [i, i, i, i]
         L.attn_bwd_workspace_size.restype = sz
@@ -136,6 +138,29 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, window: 
                                     int(bool(causal)), float(scale or 0.0), int(window),
                                     ctypes.c_void_p(_stream(stream)))
         _check("attn_fwd_gqa", rc)
+    return out, lse
+
+
+def attn_fwd_sparse(q, k, v, block_mask, causal: bool = False, scale: float | None = None, window: int = 0,
+                    out=None, lse=None, stream=None):
+    """bf16 forward with a block-sparse key mask: block_mask is a uint8 (or
+    bool) CUDA tensor (B, H, T, T), T = ceil(N / 128); query block i of
+    (b, h) sees key block j iff block_mask[b, h, i, j] != 0 (ANDed with the
+    causal / window masks).  Rows that see no key get O = 0, LSE = -inf."""
+    _check_qkv(q, k, v, torch.bfloat16)
+    out, lse = _outputs(q, out, lse)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    T = (N + 127) // 128
+    if block_mask.dtype == torch.bool:
+        block_mask = block_mask.to(torch.uint8)
+    if (block_mask.dtype != torch.uint8 or not block_mask.is_cuda or not block_mask.is_contiguous()
+            or tuple(block_mask.shape) != (B, H, T, T)):
+        raise ValueError(f"block_mask must be a contiguous uint8 CUDA tensor of shape ({B}, {H}, {T}, {T})")
+    rc = library().attn_fwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(block_mask), B, H, Hkv, N,
+                                   d, int(bool(causal)), float(scale or 0.0), int(window),
+                                   ctypes.c_void_p(_stream(stream)))
+    _check("attn_fwd_sparse", rc)
     return out, lse
 
 

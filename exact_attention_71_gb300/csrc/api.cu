@@ -138,10 +138,21 @@ float resolve_scale(float scale, int d) {
 
 int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
                    int N, int d, int causal, float scale, int window, const float* qs, const float* ks, const float* vs,
-                   void* stream) {
+                   void* stream, const uint8_t* block_mask = nullptr) {
     attn::FwdGeometry g;
     cudaError_t (*run)(const attn::FwdMaps&, const attn::FwdParams&, int, cudaStream_t) = nullptr;
-    if (fp8) {
+    if (block_mask) {
+        if (d == 64) {
+            g = attn::geom_sparse_d64();
+            run = attn::run_fwd_sparse_d64;
+        } else if (d == 128) {
+            g = attn::geom_sparse_d128();
+            run = attn::run_fwd_sparse_d128;
+        } else {
+            g = attn::geom_sparse_d256();
+            run = attn::run_fwd_sparse_d256;
+        }
+    } else if (fp8) {
         if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 only (got %d)", d);
         g = attn::geom_fp8_d128();
         run = attn::run_fwd_fp8_d128;
@@ -174,12 +185,15 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
     p.window = window;
     p.scale_log2 = resolve_scale(scale, d) * 1.4426950408889634f;
     p.n_mblocks = (N + g.nq * 128 - 1) / (g.nq * 128);
+    p.block_mask = block_mask;
+    p.n_tb = (N + 127) / 128;
     p.wait_limit = g_wait_limit.load();
     if ((rc = status_ptr(&p.status)) != ATTN_OK) return rc;
     int sms = 0;
     if ((rc = sm_count(&sms)) != ATTN_OK) return rc;
     cudaError_t e = run(maps, p, sms, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, fp8 ? "attn_fwd_fp8 launch" : "attn_fwd launch");
+    if (e != cudaSuccess)
+        return cuda_fail(e, block_mask ? "attn_fwd_sparse launch" : (fp8 ? "attn_fwd_fp8 launch" : "attn_fwd launch"));
     return ATTN_OK;
 }
 
@@ -259,6 +273,19 @@ int attn_fp8_prep_rope(const void* x, void* x8, float* scales, const float* rope
                                        interleaved ? 2 : 1, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_fp8_prep_rope launch");
     return ATTN_OK;
+}
+
+int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse, const unsigned char* block_mask,
+                    int B, int H, int H_kv, int N, int d, int causal, float scale, int window, void* stream) {
+    g_err[0] = '\0';
+    int rc = check_common(q, k, v, o, lse, B, H, N, d, window);
+    if (rc != ATTN_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    if (!block_mask) return fail(ATTN_ERR_INVALID_ARG, "null block mask");
+    return launch_forward(false, q, k, v, o, lse, B, H, H_kv, N, d, causal, scale, window, nullptr, nullptr, nullptr,
+                          stream, block_mask);
 }
 
 size_t attn_bwd_workspace_size(int B, int H, int N, int d) {

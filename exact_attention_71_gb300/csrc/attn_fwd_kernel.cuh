@@ -49,6 +49,8 @@ struct FwdParams {
     int causal, window;
     float scale_log2;        // softmax scale * log2(e)
     int n_mblocks;           // ceil(N / (NQ * 128))
+    const uint8_t* block_mask;   // block-sparse only: (B, H, n_tb, n_tb), nonzero = visible
+    int n_tb;                    // ceil(N / 128): 128 x 128 mask blocks per side
     unsigned long long wait_limit;
     int* status;             // device status word (first failing site)
 };
@@ -66,8 +68,9 @@ enum : int {
     SITE_TURN = 0x41,
 };
 
-template <int D_, int BN_, int NQ_, bool FP8_>
+template <int D_, int BN_, int NQ_, bool FP8_, bool SPARSE_ = false>
 struct FwdCfg {
+    static constexpr bool SPARSE = SPARSE_;               // block-sparse key mask
     static constexpr int D = D_;
     static constexpr int BN = BN_;
     static constexpr int NQ = NQ_;
@@ -96,7 +99,7 @@ struct FwdCfg {
     // Issuer warps: one per query tile where the tile's MMAs are long enough
     // (bf16, d = 128) for the hand-off latency to dominate; one warp for both
     // tiles where the softmax is the longer phase (FP8, d = 64) or NQ = 1.
-    static constexpr int MMA_WARPS = (!FP8 && D == 128 && NQ == 2) ? 2 : 1;
+    static constexpr int MMA_WARPS = (!FP8 && !SPARSE && D == 128 && NQ == 2) ? 2 : 1;
     static constexpr int THREADS = NQ * 128 + 128;
     static constexpr int BAR_BYTES = 256;
     // The reference maximum of a row moves only when the row maximum exceeds
@@ -207,13 +210,67 @@ __device__ __forceinline__ void item_coords(const FwdParams& p, int item, int& m
     }
 }
 
+// The key tiles of an item.  Query tile t sees key tiles [lo[t], hi[t]]
+// (causal / window ranges), and with a block-sparse mask only those whose
+// 128 x 128 mask block is set; first[t] / last[t] are its first and last
+// visible key tile (-1 when it sees none, which makes the tile inactive).
+// The roles walk the union of the active tiles' sets in increasing order;
+// -1 ends a walk.
 template <int NQ>
 struct WorkItem {
     int b, h, bh, q0;
     int lo[NQ], hi[NQ];
+    int first[NQ], last[NQ];
     bool active[NQ];
-    int u_lo, u_hi;       // union of the active tiles' key-tile ranges
+    bool in_n[NQ];        // query tile starts inside the sequence
+    const uint8_t* mrow[NQ];
+    int u_lo, u_hi;       // first and last key tile of the union (-1: none)
 };
+
+template <class Cfg>
+__device__ __forceinline__ bool key_in_tile(const WorkItem<Cfg::NQ>& w, int t, int u) {
+    if (u < w.lo[t] || u > w.hi[t]) return false;
+    if constexpr (Cfg::SPARSE) return __ldg(w.mrow[t] + ((u * Cfg::BN) >> 7)) != 0;
+    return true;
+}
+
+// Next key tile after u in the union of the active tiles' sets, or -1.
+template <class Cfg>
+__device__ __forceinline__ int next_key(const WorkItem<Cfg::NQ>& w, int u) {
+    if constexpr (!Cfg::SPARSE) return u < w.u_hi ? u + 1 : -1;
+    for (int x = u + 1; x <= w.u_hi; ++x) {
+#pragma unroll
+        for (int t = 0; t < Cfg::NQ; ++t)
+            if (w.active[t] && key_in_tile<Cfg>(w, t, x)) return x;
+    }
+    return -1;
+}
+
+// One query tile's part of an item, for roles that index the tile at run
+// time (a register copy instead of a dynamically indexed array).
+struct TileKeys {
+    int lo, hi, first, last;
+    bool active, in_n;
+    const uint8_t* mrow;
+};
+
+template <class Cfg>
+__device__ __forceinline__ TileKeys tile_keys(const WorkItem<Cfg::NQ>& w, int t) {
+    TileKeys k{w.lo[0], w.hi[0], w.first[0], w.last[0], w.active[0], w.in_n[0], w.mrow[0]};
+#pragma unroll
+    for (int x = 1; x < Cfg::NQ; ++x)
+        if (t == x) k = TileKeys{w.lo[x], w.hi[x], w.first[x], w.last[x], w.active[x], w.in_n[x], w.mrow[x]};
+    return k;
+}
+
+// Next key tile after u in the tile's set, or -1.
+template <class Cfg>
+__device__ __forceinline__ int next_in(const TileKeys& k, int u) {
+    if constexpr (!Cfg::SPARSE) return u < k.last ? u + 1 : -1;
+    for (int x = u + 1; x <= k.last; ++x)
+        if (__ldg(k.mrow + ((x * Cfg::BN) >> 7)) != 0) return x;
+    return -1;
+}
 
 template <class Cfg>
 __device__ __forceinline__ WorkItem<Cfg::NQ> decode_item(const FwdParams& p, int item) {
@@ -223,19 +280,33 @@ __device__ __forceinline__ WorkItem<Cfg::NQ> decode_item(const FwdParams& p, int
     w.b = w.bh / p.H;
     w.h = w.bh % p.H;
     w.q0 = mb * Cfg::NQ * Cfg::BM;
+    w.u_lo = -1;
+    w.u_hi = -1;
 #pragma unroll
     for (int t = 0; t < Cfg::NQ; ++t) {
-        w.active[t] = (w.q0 + t * Cfg::BM) < p.N;
-        tile_range<Cfg>(p, w.q0 + t * Cfg::BM, w.lo[t], w.hi[t]);
-    }
-    w.u_lo = w.lo[0];
-    w.u_hi = w.hi[0];
-#pragma unroll
-    for (int t = 1; t < Cfg::NQ; ++t)
-        if (w.active[t]) {
-            w.u_lo = min(w.u_lo, w.lo[t]);
-            w.u_hi = max(w.u_hi, w.hi[t]);
+        const int qs = w.q0 + t * Cfg::BM;
+        w.in_n[t] = qs < p.N;
+        tile_range<Cfg>(p, qs, w.lo[t], w.hi[t]);
+        w.mrow[t] = nullptr;
+        w.first[t] = w.lo[t];
+        w.last[t] = w.hi[t];
+        if constexpr (Cfg::SPARSE) {
+            w.mrow[t] = p.block_mask + (static_cast<size_t>(w.bh) * p.n_tb + min(qs, p.N - 1) / 128) * p.n_tb;
+            w.first[t] = -1;
+            w.last[t] = -1;
+            if (w.in_n[t]) {
+                for (int x = w.lo[t]; x <= w.hi[t]; ++x)
+                    if (key_in_tile<Cfg>(w, t, x)) { w.first[t] = x; break; }
+                for (int x = w.hi[t]; x >= w.lo[t] && w.first[t] >= 0; --x)
+                    if (key_in_tile<Cfg>(w, t, x)) { w.last[t] = x; break; }
+            }
         }
+        w.active[t] = w.in_n[t] && w.first[t] >= 0 && w.first[t] <= w.last[t];
+        if (w.active[t]) {
+            w.u_lo = w.u_lo < 0 ? w.first[t] : min(w.u_lo, w.first[t]);
+            w.u_hi = max(w.u_hi, w.last[t]);
+        }
+    }
     return w;
 }
 
@@ -399,14 +470,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tma_load_4d(sQ + t * Cfg::Q_TILE_BYTES + cb * (BM * 128), &tmap_q, &bars->q_full[t],
                                     cb * Cfg::BOX_ELEMS, w.h, w.q0 + t * BM, w.b, pol_q);
                 }
-                // Step u in [u_lo, u_hi + 1]: K_u (if u <= u_hi) and V_{u-1} (if u > u_lo).
-                for (int u = w.u_lo; u <= w.u_hi + 1 && ok; ++u) {
+                // Steps over the item's key tiles u (in order) and one more:
+                // each loads K_u (while there is a u) and V of the previous u.
+                for (int u = w.u_lo, prev = -1; ok && (u >= 0 || prev >= 0);) {
                     const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
                     if (!wait_phase(&bars->ring_empty[stage], (round & 1) ^ 1, abort_flag, p, SITE_LOAD_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    const bool with_k = u <= w.u_hi, with_v = u > w.u_lo;
+                    const bool with_k = u >= 0, with_v = prev >= 0;
                     mbar_arrive_expect_tx(&bars->ring_full[stage],
                                           (with_k ? Cfg::KV_TILE_BYTES : 0) + (with_v ? Cfg::KV_TILE_BYTES : 0));
                     uint8_t* dst = sKV + stage * Cfg::STAGE_BYTES;
@@ -420,9 +492,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                         for (int cb = 0; cb < Cfg::NCB; ++cb)
                             tma_load_4d(dst + Cfg::KV_TILE_BYTES + cb * (BN * 128), &tmap_v, &bars->ring_full[stage],
-                                        cb * Cfg::BOX_ELEMS, w.h / p.group, (u - 1) * BN, w.b, pol_kv);
+                                        cb * Cfg::BOX_ELEMS, w.h / p.group, prev * BN, w.b, pol_kv);
                     }
                     ++it;
+                    prev = u;
+                    u = u >= 0 ? next_key<Cfg>(w, u) : -1;
                 }
             }
             // Let every copy this warp issued land before the CTA can exit (on
@@ -474,7 +548,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     ++qn[t];
                 }
             }
-            for (int u = w.u_lo; u <= w.u_hi + 1 && ok; ++u) {
+            for (int u = w.u_lo, prev = -1; ok && (u >= 0 || prev >= 0); prev = u, u = u >= 0 ? next_key<Cfg>(w, u) : -1) {
                 const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
                 ++it;
                 if (!warp_wait(&bars->ring_full[stage], round & 1, abort_flag, p, SITE_MMA_FULL)) {
@@ -488,14 +562,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
                     if (t % MW != wi || !w.active[t]) continue;
-                    const bool do_pv = u - 1 >= w.lo[t] && u - 1 <= w.hi[t];
-                    const bool do_s = u <= w.hi[t] && u >= w.lo[t];
+                    const bool do_pv = prev >= 0 && key_in_tile<Cfg>(w, t, prev);
+                    const bool do_s = u >= 0 && key_in_tile<Cfg>(w, t, u);
                     if (!do_pv && !do_s) continue;
                     if (do_pv && !warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
                         ok = false;
                         break;
                     }
-                    const int k = item_base + blocks_before(w, t, u);
+                    // (the turn counter is used by the dense instantiations only,
+                    // whose walk is contiguous: the final step is u_hi + 1)
+                    const int k = item_base + blocks_before(w, t, u >= 0 ? u : prev + 1);
                     if (MW > 1 && !wait_turn(issued, k, abort_flag, p, SITE_TURN)) {
                         ok = false;
                         break;
@@ -504,13 +580,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (elect_one()) {
                         if (do_pv) {
                             issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc, !first_pv[t]);
-                            if (u - 1 == w.hi[t]) mma_commit(&bars->o_full[t]);
+                            if (prev == w.last[t]) mma_commit(&bars->o_full[t]);
                         }
                         if (do_s) {
                             issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
                             mma_commit(&bars->s_full[t]);
                             // Q_t is free for the next item once its last S MMA is done.
-                            if (u == w.hi[t]) mma_commit(&bars->q_empty[t]);
+                            if (u == w.last[t]) mma_commit(&bars->q_empty[t]);
                         }
                         if (MW > 1) {
                             __threadfence_block();
@@ -557,12 +633,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
             const int item = round_item(rnd);
             if (item >= total_items) continue;
-            int mb, bh;
-            item_coords(p, item, mb, bh);
-            const int b = bh / p.H, h = bh % p.H;
-            const int qs = mb * NQ * BM + t * BM;
-            if (qs >= p.N) continue;                         // tile t inactive for this item
+            const WorkItem<NQ> w = decode_item<Cfg>(p, item);
+            const TileKeys tk = tile_keys<Cfg>(w, t);
+            const int bh = w.bh, b = w.b, h = w.h;
+            const int qs = w.q0 + t * BM;
+            if (!tk.in_n) continue;                          // tile t beyond the sequence
             const int i = qs + r;                                  // query row
+            if (!tk.active) {
+                // Block-sparse mask: this query tile sees no key.
+                if (i < p.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                                          ((static_cast<size_t>(b) * p.N + i) * p.H + h) * D);
+#pragma unroll
+                    for (int x = 0; x < D / 8; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
+                    p.lse[static_cast<size_t>(bh) * p.N + i] = -INFINITY;
+                }
+                continue;
+            }
             // Visible keys of row i: [klo, khi].
             const int klo = p.window > 0 ? i - p.window + 1 : 0;
             const int khi = p.causal ? min(i, p.N - 1) : p.N - 1;
@@ -579,9 +666,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             float m = -INFINITY;   // reference maximum of the log2-scaled scores
             float l = 0.0f;        // running sum of exp2(score - m)
-            int my_lo, my_hi;
-            tile_range<Cfg>(p, qs, my_lo, my_hi);
-            for (int j = my_lo; j <= my_hi; ++j) {
+            bool first_tile = true;
+            for (int j = tk.first; j >= 0; j = next_in<Cfg>(tk, j)) {
                 bool wt = wait_phase(&bars->s_full[t], count & 1, abort_flag, p, SITE_SOFTMAX_S);
                 if (!__all_sync(0xffffffffu, wt)) {
                     ok = false;
@@ -628,9 +714,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // since O and l share the reference); the FP8 path tracks it
                 // exactly so that P <= 1 before the e4m3 scaling.
                 const float m_tile = mx * mult;
-                float m_use = m;
-                if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY) m_use = fmaxf(m, m_tile);
-                if (m_use == -INFINITY) m_use = 0.0f;
+                float m_new = m;
+                if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY) m_new = fmaxf(m, m_tile);
+                // A row that has seen no visible key yet keeps m = -inf (so
+                // that its first real scores set the reference, however
+                // negative); its exponent reference is then 0 and its P is 0.
+                const float m_use = m_new == -INFINITY ? 0.0f : m_new;
                 const float alpha = ex2_approx(m - m_use);
                 const float2 mult2 = make_float2(mult, mult);
                 const float2 neg2 = make_float2(-m_use, -m_use);
@@ -685,7 +774,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // Rescale the accumulator of the rows whose maximum moved.  The
                 // commit that signalled S_t(j) also covers O_t += P_t V_{j-1}, so
                 // O_t is stable here; the next P V waits for p_full below.
-                if (j > my_lo && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                if (!first_tile && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t orr[32];
@@ -700,7 +789,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&bars->p_full[t]);
-                m = m_use;
+                m = m_new;
+                first_tile = false;
                 ++count;
             }
             if (!ok) break;
@@ -711,7 +801,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             if (!ok) break;
             tc_fence_after();
-                float out_mult = 1.0f / l;
+                // l = 0 only for a row that sees no key: O = 0, LSE = -inf.
+                float out_mult = l > 0.0f ? 1.0f / l : 0.0f;
                 if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / 256.0f);
                 const bool store = i < p.N;
                 __nv_bfloat16* orow =

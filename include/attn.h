@@ -156,6 +156,23 @@ int attn_fp8_prep_rope(const void* x, void* x8, float* scales, const float* rope
                        int mode, unsigned long long sign_seed, int interleaved, void* stream);
 
 /*
+ * attn_fwd_sparse -- bf16 forward with a block-sparse key mask (the
+ * practitioner's FA3 post, §3.3 and §4.3: the caller marks which KV blocks a
+ * Q block skips; the decision is per (Q block, KV block), not per element).
+ * As attn_fwd_gqa, except that
+ *   block_mask : const uint8 (B, H, T, T), device, T = ceil(N / 128), owned
+ *                by the caller; entry [b][h][i][j] != 0 lets query rows
+ *                [128 i, 128 i + 128) of (b, h) see key rows [128 j,
+ *                128 j + 128).  It is ANDed with the causal and window masks.
+ * Key blocks a query block does not see are skipped, not computed.  A row
+ * that sees no key gets O = 0 and LSE = -inf.  d must be 64, 128 or 256.
+ * Errors: as attn_fwd_gqa; a NULL block_mask is ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const unsigned char* block_mask, int B, int H, int H_kv, int N, int d,
+                    int causal, float scale, int window, void* stream);
+
+/*
  * attn_bwd_workspace_size / attn_bwd -- backward of attn_fwd / attn_fwd_gqa
  * (deep-reading report §3.4: FA3 keeps FA2's recompute strategy; five
  * matrix products against the forward's two).  For a loss L with upstream

@@ -114,3 +114,12 @@ def test_backward_arguments_checked(lib):
     assert b"256-byte" in lib.attn_last_error_string()
     assert f(*args(wsb=ws - 1)) == -1
     assert b"smaller" in lib.attn_last_error_string()
+
+
+def test_sparse_arguments_checked(lib):
+    f = lib.attn_fwd_sparse
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 2, 2, 100, 128, 0, 0.0, 0, None) == -1
+    assert b"mask" in lib.attn_last_error_string()
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 3, 100, 128, 0, 0.0, 0, None) == -1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 100, 96, 0, 0.0, 0, None) == -2
+    assert f(None, None, None, None, None, None, 1, 2, 2, 0, 128, 0, 0.0, 0, None) == 0

@@ -141,3 +141,26 @@ def test_growing_scores_exercise_rescaling(causal):
     # LSE here reaches ~100: the tolerance is relative to its magnitude
     assert e["rms"] <= 2e-3 and e["max_excess"] <= 1e-2, e
     assert np.max(np.abs(lse_rows(lse, rows) - lse_ref) / np.maximum(1.0, np.abs(lse_ref))) <= 1e-5, e
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_window_rows_whose_first_key_tile_is_masked_with_very_negative_scores(d):
+    """Causal, W = 200, N = 640: rows 583..639 see none of the keys of their
+    query tile's first key tile.  Every score is -16 sqrt(d) (q = 4, k = -4),
+    far below 0, so the row's first visible scores must set its running
+    maximum (a maximum left at 0 would underflow every P).  Constant scores:
+    O_i is the mean of the visible V rows (and the oracle agrees)."""
+    B, N, H, W = 1, 640, 1, 200
+    q = np.full((B, N, H, d), synth.to_bf16_bits(np.array([4.0]))[0], dtype=np.uint16)
+    k = np.full((B, N, H, d), synth.to_bf16_bits(np.array([-4.0]))[0], dtype=np.uint16)
+    v = synth.tensor_bf16((B, N, H, d), seed=3, stream=3)
+    o, lse = api.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=True, window=W)
+    torch.cuda.synchronize()
+    rows = np.arange(N, dtype=np.int32)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True, window=W, rows=rows)
+    vf = synth.bf16_bits_to_f32(v).astype(np.float64)
+    for i in (0, 582, 583, 600, 639):
+        np.testing.assert_allclose(o_ref[0, 0, i], vf[0, max(0, i - W + 1):i + 1, 0].mean(axis=0), atol=1e-12)
+    e = errors(gpu_rows(o, rows), o_ref, lse_rows(lse, rows), lse_ref)
+    assert_bf16_parity(e, f"masked first tile d={d}")
+    assert api.device_status()[0] == 0
