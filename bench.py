@@ -53,7 +53,40 @@ WORKLOADS = {
                 window=0, dtype="bf16", direction="bwd"),
     "bwd_c2": dict(name="bf16 bwd B=2 H=32 N=4096 d=128 causal", B=2, H=32, N=4096, d=128, causal=True, window=0,
                    dtype="bf16", direction="bwd"),
+    # Block-sparse forward: a band of +-8 key blocks around the diagonal plus
+    # every 8th key block (128 x 128 blocks; about 24 % of them visible).
+    "sparse": dict(name="bf16 fwd block-sparse B=1 H=16 N=16384 d=128 non-causal, band +-8 blocks + every 8th block",
+                   B=1, H=16, N=16384, d=128, causal=False, window=0, dtype="bf16", sparse="band8_stride8"),
 }
+
+
+def block_mask(w: dict) -> np.ndarray:
+    """The workload's block mask (B, H, T, T), uint8."""
+    T = (w["N"] + 127) // 128
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    if w.get("sparse") != "band8_stride8":
+        raise SystemExit(f"unknown block pattern {w.get('sparse')}")
+    m = ((np.abs(i - j) <= 8) | (j % 8 == 0)).astype(np.uint8)
+    return np.ascontiguousarray(np.broadcast_to(m, (w["B"], w["H"], T, T)))
+
+
+def visible_pairs(w: dict, rows=None) -> int:
+    """Exact number of (query, key) pairs that take part, over all heads
+    (block mask, causal and window), for all query rows or the given ones."""
+    N = w["N"]
+    rows = np.arange(N, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    lo = np.maximum(0, rows - w["window"] + 1) if w["window"] > 0 else np.zeros(len(rows), dtype=np.int64)
+    hi = rows if w["causal"] else np.full(len(rows), N - 1)
+    if not w.get("sparse"):
+        return int(np.sum(hi - lo + 1)) * w["B"] * w["H"]
+    m = block_mask(w)[0, 0].astype(bool)          # the pattern is the same for every head
+    keys = np.arange(N)
+    total = 0
+    for r, a, b in zip(rows, lo, hi):
+        kb = m[r // 128][keys[a:b + 1] // 128]
+        total += int(np.count_nonzero(kb))
+    return total * w["B"] * w["H"]
 
 
 def workload(spec: str) -> dict:
@@ -87,6 +120,8 @@ def flops_per_step(w: dict) -> float:
     against two, the pages' convention)."""
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     mult = 2.5 if w.get("direction") == "bwd" else 1.0
+    if w.get("sparse"):
+        return mult * 4.0 * d * visible_pairs(w)
     if w["window"] > 0:
         return mult * 4.0 * B * H * d * attended_pairs(N, w["causal"], w["window"])
     return mult * 4.0 * B * H * N * N * d / (2.0 if w["causal"] else 1.0)
@@ -120,6 +155,7 @@ KERNEL_SOURCES = {
     "attn_fwd_fp8": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d128.cu"),
     "fp8_prep": ("fp8_prep.cu", "fp8_prep.cuh"),
     "attn_bwd": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_bwd_kernel.cuh", "attn_bwd.cu", "attn_bwd.cuh"),
+    "attn_fwd_sparse": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_sparse_d128.cu"),
 }
 
 
@@ -281,12 +317,11 @@ def _oracle_run(w, arrs, size, cores):
         return t, flops, f"{nh} of {H} query heads in full x {B} batch ({flops / 1e9:.2f} GFLOP, fp64, {cores} threads)"
     q, k, v = arrs[:3]
     rows = synth.sample_rows(N, size, seed=17)
-    oracle.attention(q, k, v, causal=w["causal"], window=w["window"], rows=rows, nthreads=cores)
+    bm = block_mask(w) if w.get("sparse") else None
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=w["causal"], window=w["window"], rows=rows, nthreads=cores, block_mask=bm)
     t = time.perf_counter() - t0
-    rows = np.asarray(rows, dtype=np.int64)
-    hi = rows if w["causal"] else np.full(len(rows), N - 1)
-    lo = np.maximum(0, rows - w["window"] + 1) if w["window"] > 0 else np.zeros(len(rows), dtype=np.int64)
-    flops = 4.0 * d * int(np.sum(hi - lo + 1)) * B * H
+    flops = 4.0 * d * visible_pairs(w, rows)
     return t, flops, f"{len(rows)} seeded query rows per head x all {B * H} heads ({flops / 1e9:.2f} GFLOP, fp64, {cores} threads)"
 
 
@@ -449,6 +484,8 @@ def main():
         if w["dtype"] == "fp8":
             q8, k8, v8, qs, ks, vs = api.fp8_prepare_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, sign_seed=1234)
             sets.append((q8, k8, v8, qs, ks, vs))
+        elif w.get("sparse"):
+            sets.append((q, k, v, torch.from_numpy(block_mask(w)).to(device)))
         elif bwd:
             # The backward consumes the forward's O and LSE, computed once here.
             o_s, lse_s = api.attn_fwd(q, k, v, causal=w["causal"], window=w["window"])
@@ -471,6 +508,8 @@ def main():
         elif bwd:
             api.attn_bwd(*s, causal=w["causal"], window=w["window"], dq=grads[0], dk=grads[1], dv=grads[2],
                          workspace=work, stream=stream)
+        elif w.get("sparse"):
+            api.attn_fwd_sparse(*s, causal=w["causal"], window=w["window"], out=o, lse=lse, stream=stream)
         else:
             api.attn_fwd(*s, causal=w["causal"], window=w["window"], out=o, lse=lse, stream=stream)
 
@@ -499,7 +538,8 @@ def main():
     value = ws * flops * args.steps / (ms_total / 1e3) / 1e12
     peaks, peak_src = load_peaks()
     achieved = flops / (ms_step / 1e3) / 1e12
-    kernel = "attn_fwd_fp8" if w["dtype"] == "fp8" else ("attn_bwd" if bwd else "attn_fwd")
+    kernel = "attn_fwd_fp8" if w["dtype"] == "fp8" else ("attn_bwd" if bwd else
+                                                         ("attn_fwd_sparse" if w.get("sparse") else "attn_fwd"))
     if w["dtype"] == "fp8":
         fp8_peak = peaks.get("fp8_tflops") or 2.0 * peaks["bf16_tflops"]
         peak, peak_note = fp8_peak, f"{peak_src} bf16 burst x 2 (nominal fp8:bf16 ratio)"
@@ -518,7 +558,9 @@ def main():
             "config": {"workload": w["name"], "B": B, "H": H, "H_kv": w.get("Hkv", H), "N": N, "d": d,
                        "causal": w["causal"],
                        "window": w["window"], "flops_per_step": flops,
-                       "flop_convention": "4 B H N^2 d, halved for causal; window: 4 d x attended pairs",
+                       "flop_convention": ("4 d x visible (query, key) pairs after the block mask" if w.get("sparse")
+                                           else "4 B H N^2 d, halved for causal; window: 4 d x attended pairs")
+                                          + ("; backward 2.5 x" if bwd else ""),
                        "l2": "inputs larger than L2 (two resident input sets, alternated per step)",
                        "global_batch": global_batch,
                        "parallelism": f"batch shards x{ws}, no collective on the data path"},
@@ -547,6 +589,8 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
     import torch
     if w.get("direction") == "bwd":
         return e2e_measure_bwd(api, w, device, stream, arrs, flops, steps)
+    hmask = torch.from_numpy(block_mask(w)).pin_memory() if w.get("sparse") else None
+    dmask = torch.empty_like(hmask, device=device) if hmask is not None else None
     hq, hk, hv = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in arrs)
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     dq, dk, dv = (torch.empty_like(t, device=device) for t in (hq, hk, hv))
@@ -567,6 +611,10 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
                                                              stream=stream)
                 api.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=w["causal"], window=w["window"], out=do,
                                  lse=dl, stream=stream)
+            elif hmask is not None:
+                dmask.copy_(hmask, non_blocking=True)
+                api.attn_fwd_sparse(dq, dk, dv, dmask, causal=w["causal"], window=w["window"], out=do, lse=dl,
+                                    stream=stream)
             else:
                 api.attn_fwd(dq, dk, dv, causal=w["causal"], window=w["window"], out=do, lse=dl, stream=stream)
             ho.copy_(do, non_blocking=True)
@@ -576,7 +624,7 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
         step()
     torch.cuda.synchronize(device)
     ms = time_loop(step, steps, stream) / steps
-    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + (hmask.numel() if hmask is not None else 0)
     d2h = ho.numel() * 2 + hl.numel() * 4
     return {"value": round(flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "kernel_launches_per_step": launches}

@@ -77,7 +77,7 @@ def test_all_ones_mask_equals_dense_forward():
 
 def test_full_size_band_plus_strided_pattern_sampled_rows():
     """B=1, H=16, N=16384, d=128, non-causal: a band of +-8 key blocks around
-    the diagonal plus every 8th key block (about 17 % of the blocks)."""
+    the diagonal plus every 8th key block (about 24 % of the blocks)."""
     B, N, H, d = 1, 16384, 16, 128
     T = N // 128
     i = np.arange(T)[:, None]
