@@ -62,6 +62,10 @@ def library() -> ctypes.CDLL:
         L.attn_bwd_workspace_size.restype = sz
         L.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, sz, i, i, i, i, i, i, f, i, P]
         L.attn_bwd.restype = i
+        L.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, f, i, P]
+        L.attn_bwd_noalloc.restype = i
+        L.attn_bwd_noalloc_max_scratch.argtypes = []
+        L.attn_bwd_noalloc_max_scratch.restype = sz
         L.attn_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         L.attn_device_status.restype = i
         L.attn_set_wait_limit.argtypes = [u64]
@@ -195,6 +199,25 @@ def attn_bwd(dout, q, k, v, out, lse, causal: bool = False, scale: float | None 
                             _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
                             int(bool(causal)), float(scale or 0.0), int(window), ctypes.c_void_p(_stream(stream)))
     _check("attn_bwd", rc)
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(dout, q, k, v, out, lse, causal: bool = False, scale: float | None = None, window: int = 0,
+                     dq=None, dk=None, dv=None, stream=None):
+    """attn_bwd without a workspace: the library's built-in device scratch
+    buffer is used instead (for callers that may not allocate; calls on one
+    device must not overlap on the GPU).  dq, dk, dv are allocated here only
+    when not given."""
+    _check_qkv(q, k, v, torch.bfloat16)
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    rc = library().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), B, H, Hkv, N, d, int(bool(causal)), float(scale or 0.0),
+                                    int(window), ctypes.c_void_p(_stream(stream)))
+    _check("attn_bwd_noalloc", rc)
     return dq, dk, dv
 
 

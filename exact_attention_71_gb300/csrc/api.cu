@@ -372,3 +372,67 @@ int attn_set_wait_limit(unsigned long long cycles) {
 const char* attn_last_error_string(void) { return g_err; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// attn_bwd_noalloc: the backward for callers that cannot allocate device
+// memory (see include/attn.h).  Its scratch -- the LSE / D rows and the
+// float32 dQ accumulator that attn_bwd keeps in the caller's workspace -- is
+// this file-scope array, created once per device when the library's device
+// code is loaded there and held until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(256) << 20;   // 256 MiB
+static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
+
+void* g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mutex;
+
+// Device address of g_bwd_scratch on the current device (host code may not
+// use the array's name as a device address).  Looked up once per device.
+int scratch_ptr(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(backward scratch)");
+        g_scratch_ptr[dev] = ptr;
+    }
+    *out = g_scratch_ptr[dev];
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_bwd_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, int causal, float scale,
+                     int window, void* stream) {
+    g_err[0] = '\0';
+    if (B < 0 || H < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d N=%d)", B, H, N);
+    if (d == 128 && static_cast<long long>(B) * H * N > 0) {
+        const size_t need = attn_bwd_workspace_size(B, H, N, d);
+        if (need > kNoAllocScratchBytes)
+            return fail(ATTN_ERR_INVALID_ARG,
+                        "attn_bwd_noalloc: this problem needs %zu bytes of scratch, more than the built-in %zu "
+                        "(4 * B * H * ceil(N / 128) * 128 * (d + 2) bytes must fit); use attn_bwd with a workspace",
+                        need, kNoAllocScratchBytes);
+    }
+    void* scratch = nullptr;
+    if (static_cast<long long>(B) * H * N > 0) {
+        const int rc = scratch_ptr(&scratch);
+        if (rc != ATTN_OK) return rc;
+    }
+    // The prep launch of attn_bwd rewrites every scratch entry the call reads
+    // (it zeroes the dQ accumulator), so nothing left by an earlier call leaks in.
+    return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, scratch, kNoAllocScratchBytes, B, H, H_kv, N, d, causal, scale,
+                    window, stream);
+}
+
+}  // extern "C"

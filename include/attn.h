@@ -208,6 +208,35 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              float scale, int window, void* stream);
 
 /*
+ * attn_bwd_noalloc / attn_bwd_noalloc_max_scratch -- attn_bwd for callers
+ * that cannot allocate device memory: code running where cudaMalloc is not
+ * allowed or not wanted (inside a framework's own allocator or memory pool,
+ * in a process whose memory budget is fixed up front, or in a library layer
+ * that must not own device buffers).  There is no counterpart in the paper;
+ * this is a convenience of this library.
+ * Arguments as attn_bwd, without the workspace: the scratch (about
+ * 4 * B * H * ceil(N / 128) * 128 * (d + 2) bytes, attn_bwd_workspace_size)
+ * lives in one static device buffer of attn_bwd_noalloc_max_scratch() bytes
+ * (256 MiB), created on every GPU that loads this library's device code and
+ * held until the process exits.  A larger problem is rejected with
+ * ATTN_ERR_INVALID_ARG and a message naming the sizes; attn_bwd with a
+ * caller workspace has no such limit.
+ *  - The first call on a device looks up the buffer's device address (one
+ *    cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call on a device shares the one buffer: calls whose kernels can
+ *    overlap on the GPU (different streams without ordering) race and give
+ *    wrong gradients.  Order them on one stream.  Each call rewrites the
+ *    parts it reads first (the dQ accumulator is zeroed), so sequential
+ *    calls are independent.
+ *  - Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ *    call.
+ */
+size_t attn_bwd_noalloc_max_scratch(void);
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, int B, int H, int H_kv,
+                     int N, int d, int causal, float scale, int window, void* stream);
+
+/*
  * attn_device_status -- waits for `stream`, then reads and clears the
  * library's device status word.  Every wait inside the kernels is bounded;
  * a kernel that gives up records the site in this word and returns instead
