@@ -115,6 +115,34 @@ int make_map(CUtensorMap* map, const void* base, int B, int H, int N, int d, int
     return ATTN_OK;
 }
 
+// bf16 (B, N, H, d) tensor as 4-D {d, H, N, B}; box = whole rows (d
+// elements) of 128 tokens of one head, no swizzle: the FP8 prep's tile.
+int make_row_map(CUtensorMap* map, const void* base, int B, int H, int N, int d) {
+    auto enc = encode_fn();
+    if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
+                             static_cast<cuuint64_t>(N) * H * d * 2};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, 128, 1};
+    cuuint32_t estride[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled (rows) failed (CUresult %d)", static_cast<int>(r));
+    return ATTN_OK;
+}
+
+// Everything the prep launch needs besides its arguments.
+int prep_launch(const void* x, int B, int H, int N, int d, CUtensorMap* map, attn::PrepLaunch* L) {
+    int rc = make_row_map(map, x, B, H, N, d);
+    if (rc != ATTN_OK) return rc;
+    if ((rc = sm_count(&L->num_sms)) != ATTN_OK) return rc;
+    if ((rc = status_ptr(&L->status)) != ATTN_OK) return rc;
+    L->wait_limit = g_wait_limit.load();
+    return ATTN_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int N,
@@ -251,7 +279,11 @@ int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, i
     if (!x || !x8 || !scales) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(x) || !aligned16(x8) || !aligned16(scales))
         return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-    cudaError_t e = attn::run_fp8_prep(x, x8, scales, B, H, N, d, mode, sign_seed, is_v != 0, nullptr, nullptr, 0,
+    CUtensorMap map;
+    attn::PrepLaunch L;
+    int rc = prep_launch(x, B, H, N, d, &map, &L);
+    if (rc != ATTN_OK) return rc;
+    cudaError_t e = attn::run_fp8_prep(map, x8, scales, B, H, N, d, mode, sign_seed, is_v != 0, nullptr, nullptr, 0, L,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_fp8_prep launch");
     return ATTN_OK;
@@ -269,8 +301,12 @@ int attn_fp8_prep_rope(const void* x, void* x8, float* scales, const float* rope
     if (!x || !x8 || !scales || !rope_cos || !rope_sin) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(x) || !aligned16(x8) || !aligned16(scales) || !aligned16(rope_cos) || !aligned16(rope_sin))
         return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-    cudaError_t e = attn::run_fp8_prep(x, x8, scales, B, H, N, d, mode, sign_seed, false, rope_cos, rope_sin,
-                                       interleaved ? 2 : 1, static_cast<cudaStream_t>(stream));
+    CUtensorMap map;
+    attn::PrepLaunch L;
+    int rc = prep_launch(x, B, H, N, d, &map, &L);
+    if (rc != ATTN_OK) return rc;
+    cudaError_t e = attn::run_fp8_prep(map, x8, scales, B, H, N, d, mode, sign_seed, false, rope_cos, rope_sin,
+                                       interleaved ? 2 : 1, L, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_fp8_prep_rope launch");
     return ATTN_OK;
 }

@@ -541,7 +541,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int t = 0; t < T && ok; ++t) {
             const int h = w.head(t, p.group);
             const int q0 = w.q0(t, BM);
-            if (!bwait_warp(&bars->dq_full, t & 1, abort_flag, p, BSITE_DQ_FULL)) { ok = false; break; }
+            const bool got = bwait_warp(&bars->dq_full, t & 1, abort_flag, p, BSITE_DQ_FULL);
+            // The staging buffer of this step was last read by the bulk add of
+            // step t - 2; at most one (step t - 1's) may still be reading.
+            if (leader) bulk_wait_group_read<1>();
+            // One decision for the four warps (a warp that gave up must not
+            // leave the others waiting at the barriers below); the barrier
+            // also tells everyone that the staging buffer is free.
+            if (!named_barrier_and(1, 128, got)) { ok = false; break; }
             tc_fence_after();
             uint32_t a[BM];
 #pragma unroll
@@ -551,11 +558,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int c = 0; c < BM / 32; ++c) reg_fence32(a + c * 32);
             tc_fence_before();
             mbar_arrive(&bars->dq_empty);
-            // The staging buffer of this step was last read by the bulk add of
-            // step t - 2; at most one (step t - 1's) may still be reading.
             float* stage = reinterpret_cast<float*>(sDQ + (t & 1) * Cfg::DQ_STAGE);
-            if (leader) bulk_wait_group_read<1>();
-            named_barrier(1, 128);
 #pragma unroll
             for (int x = 0; x < BM; ++x) stage[x * D + r] = __uint_as_float(a[x]);
             fence_proxy_async_smem();

@@ -49,6 +49,21 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Barrier `id` among `count` threads that also ANDs a predicate over them:
+// every thread gets true only if every participating thread passed true.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // Instruction descriptor for kind::f16 with both operand majors given
 // (0 = K-major, 1 = MN-major); fields as in make_idesc.
 __host__ __device__ constexpr uint32_t make_idesc_ab(uint32_t ab_format, uint32_t M, uint32_t N, uint32_t a_mn,

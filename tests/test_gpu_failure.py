@@ -1,10 +1,11 @@
 """Failure detection on the GPU without a GPU fault.
 
-Every barrier wait inside the forward kernel is bounded.  The test makes
-the waits run out by setting a one-cycle wait limit: the kernel must give
-up, record the site in the library's status word and return (no hang), the
-host must see ATTN_ERR_DEVICE_TIMEOUT, and the CUDA context must stay usable
-so that the next call, with the default limit, is correct.
+Every barrier wait inside the kernels (forward, backward, FP8 prep) is
+bounded.  The tests make the waits run out by setting a one-cycle wait
+limit: the kernel must give up, record the site in the library's status word
+and return (no hang), the host must see ATTN_ERR_DEVICE_TIMEOUT, and the CUDA
+context must stay usable so that the next call, with the default limit, is
+correct.
 """
 import numpy as np
 import pytest
@@ -17,7 +18,10 @@ from tests.helpers import assert_bf16_parity, errors, gpu_rows, lse_rows, to_dev
 pytestmark = pytest.mark.gpu
 
 ATTN_ERR_DEVICE_TIMEOUT = -4
-KNOWN_SITES = {0x11, 0x12, 0x21, 0x22, 0x23, 0x24, 0x31, 0x32, 0x41}
+FWD_SITES = {0x11, 0x12, 0x21, 0x22, 0x23, 0x24, 0x31, 0x32, 0x41}
+BWD_SITES = {0x51, 0x52, 0x61, 0x62, 0x63, 0x64, 0x65, 0x66, 0x71, 0x72, 0x73, 0x74, 0x81, 0x82}
+PREP_SITES = {0x91}
+KNOWN_SITES = FWD_SITES
 
 
 def test_wait_timeout_is_reported_and_the_context_survives():
@@ -44,3 +48,49 @@ def test_wait_timeout_is_reported_and_the_context_survives():
     o_ref, lse_ref = oracle.attention(q, k, v, causal=True)
     assert_bf16_parity(errors(gpu_rows(o, rows), o_ref, lse_rows(lse, rows), lse_ref), "after timeout")
     assert api.device_status()[0] == 0
+
+
+def _timeout_then_recover(run):
+    lib = api.library()
+    assert api.device_status()[0] == 0
+    assert lib.attn_set_wait_limit(1) == 0
+    try:
+        run()
+        rc, site = api.device_status()
+    finally:
+        lib.attn_set_wait_limit(0)
+    assert api.device_status()[0] == 0
+    return rc, site
+
+
+def test_backward_wait_timeout_is_reported_and_the_context_survives():
+    B, N, H, d = 1, 700, 2, 128
+    q, k, v = synth.qkv_bf16(B, N, H, d, seed=9)
+    do = synth.tensor_bf16((B, N, H, d), seed=9, stream=4)
+    qd, kd, vd, dod = (to_dev(x) for x in (q, k, v, do))
+    o, lse = api.attn_fwd(qd, kd, vd, causal=True)
+    want = api.attn_bwd(dod, qd, kd, vd, o, lse, causal=True)
+    torch.cuda.synchronize()
+    rc, site = _timeout_then_recover(lambda: api.attn_bwd(dod, qd, kd, vd, o, lse, causal=True))
+    assert rc in (0, ATTN_ERR_DEVICE_TIMEOUT), rc
+    if rc != 0:
+        assert site in BWD_SITES, hex(site)
+    got = api.attn_bwd(dod, qd, kd, vd, o, lse, causal=True)
+    torch.cuda.synchronize()
+    assert api.device_status()[0] == 0
+    assert torch.equal(got[1], want[1]) and torch.equal(got[2], want[2])
+    assert float((got[0].float() - want[0].float()).abs().max()) <= 1e-2 * float(want[0].float().abs().max())
+
+
+def test_prep_wait_timeout_is_reported_and_the_context_survives():
+    x = synth.tensor_bf16((2, 4096, 4, 128), seed=3, stream=1)
+    xd = to_dev(x)
+    want = api.attn_fp8_prep(xd, mode=api.MODE_BLOCK_HADAMARD, sign_seed=7)
+    torch.cuda.synchronize()
+    rc, site = _timeout_then_recover(lambda: api.attn_fp8_prep(xd, mode=api.MODE_BLOCK_HADAMARD, sign_seed=7))
+    assert rc in (0, ATTN_ERR_DEVICE_TIMEOUT), rc
+    if rc != 0:
+        assert site in PREP_SITES, hex(site)
+    got = api.attn_fp8_prep(xd, mode=api.MODE_BLOCK_HADAMARD, sign_seed=7)
+    torch.cuda.synchronize()
+    assert torch.equal(got[0], want[0]) and torch.equal(got[1], want[1])
