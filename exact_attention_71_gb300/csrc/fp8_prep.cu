@@ -229,21 +229,25 @@ __global__ void __launch_bounds__(WARPS * 32)
                         }
                     }
                 }
-                // Butterflies across lanes (strides E .. D/2).
+                // Butterflies across lanes (strides E .. D/2): the lower lane of
+                // a pair keeps r + other, the upper one other - r, both as one
+                // fused multiply-add by +-1 (the product is exact, so the result
+                // is the plain sum / difference, rounded once).
 #pragma unroll
                 for (int ls = 1; ls < 32; ls <<= 1) {
-                    const bool upper = (lane & ls) != 0;
+                    const float pm = (lane & ls) ? -1.0f : 1.0f;
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
                         const float other = __shfl_xor_sync(0xffffffffu, r[rr][e], ls);
-                        r[rr][e] = upper ? (other - r[rr][e]) : (r[rr][e] + other);
+                        r[rr][e] = fmaf(r[rr][e], pm, other);
                     }
                 }
                 constexpr float inv_sqrt_d = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
                 // "+ 0.0f" maps a -0 produced by a sign flip of an exact zero to +0,
-                // so a zero always encodes as the +0 code.
+                // so a zero always encodes as the +0 code; one fused multiply-add
+                // rounds the exact product once, as the separate multiply would.
 #pragma unroll
-                for (int e = 0; e < E; ++e) r[rr][e] = __fadd_rn(r[rr][e] * inv_sqrt_d, 0.0f);
+                for (int e = 0; e < E; ++e) r[rr][e] = fmaf(r[rr][e], inv_sqrt_d, 0.0f);
             }
 #pragma unroll
             for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(r[rr][e]));
