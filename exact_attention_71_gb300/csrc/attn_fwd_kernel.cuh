@@ -103,8 +103,11 @@ struct FwdCfg {
     static constexpr int THREADS = NQ * 128 + 128;
     static constexpr int BAR_BYTES = 256;
     // The reference maximum of a row moves only when the row maximum exceeds
-    // it by more than this (log2 units); 0 = exact tracking.
-    static constexpr float RESCALE_LOG2 = FP8 ? 0.0f : 8.0f;
+    // it by more than this (log2 units), so P <= 2^RESCALE_LOG2.  FP8 scales P
+    // by P8_SCALE = 2^(8 - RESCALE_LOG2) before the e4m3 cast (P * P8_SCALE
+    // <= 256 < 448, the largest e4m3 value).
+    static constexpr float RESCALE_LOG2 = FP8 ? 4.0f : 8.0f;
+    static constexpr float P8_SCALE = FP8 ? 16.0f : 1.0f;
     // Register split: the launch gives every thread LAUNCH_REGS; the load /
     // MMA warpgroup drops to LOW_REGS and the softmax warpgroups rise to
     // HIGH_REGS.  The sum stays within the launch allocation.
@@ -679,7 +682,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if constexpr (Cfg::FP8) {
                     const size_t sb = static_cast<size_t>(bh_kv) * nblk + (j * BN) / 128;
                     mult *= p.k_scale[sb];
-                    pv_mult = 256.0f * (p.v_scale[sb] / vmax);
+                    pv_mult = Cfg::P8_SCALE * (p.v_scale[sb] / vmax);
                 }
                 uint32_t sr[BN];
 #pragma unroll
@@ -803,7 +806,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc_fence_after();
                 // l = 0 only for a row that sees no key: O = 0, LSE = -inf.
                 float out_mult = l > 0.0f ? 1.0f / l : 0.0f;
-                if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / 256.0f);
+                if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / Cfg::P8_SCALE);
                 const bool store = i < p.N;
                 __nv_bfloat16* orow =
                     reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * p.N + i) * p.H + h) * D;
