@@ -53,6 +53,11 @@ WORKLOADS = {
                 window=0, dtype="bf16", direction="bwd"),
     "bwd_c2": dict(name="bf16 bwd B=2 H=32 N=4096 d=128 causal", B=2, H=32, N=4096, d=128, causal=True, window=0,
                    dtype="bf16", direction="bwd"),
+    # The pages' FP8 figure: d = 256, 16k tokens with hidden 2048 (8 heads), N = 16k.
+    "fp8_d256": dict(name="fp8 e4m3 fwd B=1 H=8 N=16384 d=256 non-causal, outliers, block scales + Hadamard", B=1, H=8,
+                     N=16384, d=256, causal=False, window=0, dtype="fp8"),
+    "fp8_d256_causal": dict(name="fp8 e4m3 fwd B=1 H=8 N=16384 d=256 causal, outliers, block scales + Hadamard", B=1, H=8,
+                            N=16384, d=256, causal=True, window=0, dtype="fp8"),
     # Block-sparse forward: a band of +-8 key blocks around the diagonal plus
     # every 8th key block (128 x 128 blocks; about 24 % of them visible).
     "sparse": dict(name="bf16 fwd block-sparse B=1 H=16 N=16384 d=128 non-causal, band +-8 blocks + every 8th block",
@@ -153,6 +158,7 @@ def cublaslt_fp8_peak():
 KERNEL_SOURCES = {
     "attn_fwd": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_bf16_d128.cu"),
     "attn_fwd_fp8": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d128.cu"),
+    "attn_fwd_fp8_d256": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d256.cu"),
     "fp8_prep": ("fp8_prep.cu", "fp8_prep.cuh"),
     "attn_bwd": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_bwd_kernel.cuh", "attn_bwd.cu", "attn_bwd.cuh"),
     "attn_fwd_sparse": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_sparse_d128.cu"),
@@ -538,8 +544,8 @@ def main():
     value = ws * flops * args.steps / (ms_total / 1e3) / 1e12
     peaks, peak_src = load_peaks()
     achieved = flops / (ms_step / 1e3) / 1e12
-    kernel = "attn_fwd_fp8" if w["dtype"] == "fp8" else ("attn_bwd" if bwd else
-                                                         ("attn_fwd_sparse" if w.get("sparse") else "attn_fwd"))
+    kernel = ("attn_fwd_fp8" + ("_d256" if w["d"] == 256 else "")) if w["dtype"] == "fp8" else (
+        "attn_bwd" if bwd else ("attn_fwd_sparse" if w.get("sparse") else "attn_fwd"))
     if w["dtype"] == "fp8":
         fp8_peak = peaks.get("fp8_tflops") or 2.0 * peaks["bf16_tflops"]
         peak, peak_note = fp8_peak, f"{peak_src} bf16 burst x 2 (nominal fp8:bf16 ratio)"

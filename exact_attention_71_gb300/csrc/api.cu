@@ -181,9 +181,15 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
             run = attn::run_fwd_sparse_d256;
         }
     } else if (fp8) {
-        if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 only (got %d)", d);
-        g = attn::geom_fp8_d128();
-        run = attn::run_fwd_fp8_d128;
+        if (d == 128) {
+            g = attn::geom_fp8_d128();
+            run = attn::run_fwd_fp8_d128;
+        } else if (d == 256) {
+            g = attn::geom_fp8_d256();
+            run = attn::run_fwd_fp8_d256;
+        } else {
+            return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 and 256 (got %d)", d);
+        }
     } else if (d == 64) {
         g = attn::geom_bf16_d64();
         run = attn::run_fwd_bf16_d64;
@@ -262,7 +268,8 @@ int attn_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o, fl
     if (H_kv <= 0 || H % H_kv != 0)
         return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
     if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
-    if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 only (got %d)", d);
+    if (d != 128 && d != 256)
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 and 256 (got %d)", d);
     if (!q_scale || !k_scale || !v_scale) return fail(ATTN_ERR_INVALID_ARG, "null scale pointer");
     return launch_forward(true, q8, k8, v8, o, lse, B, H, H_kv, N, d, causal, scale, window, q_scale, k_scale,
                           v_scale, stream);

@@ -53,6 +53,8 @@ FwdGeometry geom_bf16_d64();
 FwdGeometry geom_bf16_d128();
 FwdGeometry geom_bf16_d256();
 FwdGeometry geom_fp8_d128();
+cudaError_t run_fwd_fp8_d256(const FwdMaps&, const FwdParams&, int, cudaStream_t);
+FwdGeometry geom_fp8_d256();
 cudaError_t run_fwd_sparse_d64(const FwdMaps&, const FwdParams&, int, cudaStream_t);
 cudaError_t run_fwd_sparse_d128(const FwdMaps&, const FwdParams&, int, cudaStream_t);
 cudaError_t run_fwd_sparse_d256(const FwdMaps&, const FwdParams&, int, cudaStream_t);
