@@ -384,6 +384,32 @@ def run_reference(args, w, key):
     print(json.dumps(line), flush=True)
 
 
+def measure_spec_peak():
+    """Spec dense tensor peak pinned by this repository's own tcgen05
+    microbenchmark (csrc/peak/mma_peak.cu): SMs x measured dense FLOP per
+    clock per SM x the maximum SM clock."""
+    src = os.path.join(ROOT, "exact_attention_71_gb300", "csrc", "peak", "mma_peak.cu")
+    exe = os.path.join(ROOT, "_build", "mma_peak")
+    os.makedirs(os.path.dirname(exe), exist_ok=True)
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-o", exe, src],
+                   check=True)
+    res = json.loads(subprocess.run([exe], check=True, capture_output=True, text=True).stdout.strip())
+    mhz = res["max_sm_mhz"]
+    res["bf16_tflops_spec"] = round(res["sms"] * res["bf16_flop_per_clk_per_sm"] * mhz * 1e6 / 1e12, 1)
+    res["e4m3_tflops_spec"] = round(res["sms"] * res["e4m3_flop_per_clk_per_sm"] * mhz * 1e6 / 1e12, 1)
+    res["how"] = ("one CTA per SM issuing 4096 back-to-back 128x256 tcgen05 MMAs (both operands in shared "
+                  "memory); FLOP/clk/SM from the slowest SM's clock64 time; spec = SMs x that x max SM clock")
+    print(json.dumps(res), flush=True)
+
+
+def spec_peak():
+    try:
+        with open(os.path.join(ROOT, "profiles", "spec_dense_peak.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
 def measure_fp8_peak():
     """Dense e4m3 GEMM throughput of cuBLASLt (torch._scaled_mm, 8192^3,
     bf16 output), measured like the bf16 peak: best of 10 (burst) and back to
@@ -442,9 +468,13 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip e2e, FP8 and CPU baseline (profiling runs)")
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--fp8-peak", action="store_true", help="measure the cuBLASLt e4m3 GEMM peak and exit")
+    ap.add_argument("--spec-peak", action="store_true", help="measure the tcgen05 spec dense peak and exit")
     args = ap.parse_args()
     if args.fp8_peak:
         measure_fp8_peak()
+        return
+    if args.spec_peak:
+        measure_spec_peak()
         return
     w = workload(args.workload)
     if args.impl == "reference":
@@ -556,6 +586,10 @@ def main():
             "peak_source": peak_note,
             "frac_of_sustained": round(achieved / (peaks.get("bf16_tflops_sustained", peak) *
                                                    (2.0 if w["dtype"] == "fp8" else 1.0)), 4)}
+    sp = spec_peak()
+    if sp:
+        roof["frac_of_spec_dense"] = round(achieved / sp["e4m3_tflops_spec" if w["dtype"] == "fp8" else
+                                                       "bf16_tflops_spec"], 4)
     if w["dtype"] == "fp8" and cublaslt_fp8_peak():
         roof["frac_of_cublaslt_fp8_gemm"] = round(achieved / cublaslt_fp8_peak(), 4)
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": ws, "steps": args.steps,
