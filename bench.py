@@ -11,7 +11,8 @@ pages' Fig. 6 point (B=1, H=16, N=16384, d=128, non-causal; FLOPs 2.5 x the
 forward's) in its "bwd" object.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c2|c4|c5|gqa|bwd|bwd_c2|c3:N:d:causal|bwd:N:causal] [--quick]
+                    [--workload c2|c4|c5|gqa|bwd|bwd_c2|bwd_d64|sparse|fp8_d256|c3:N:d:causal|bwd:N:causal[:d]]
+                    [--quick]
 
 Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
 device (weak scaling, no collective on the data path); `value` is the work of
@@ -53,6 +54,8 @@ WORKLOADS = {
                 window=0, dtype="bf16", direction="bwd"),
     "bwd_c2": dict(name="bf16 bwd B=2 H=32 N=4096 d=128 causal", B=2, H=32, N=4096, d=128, causal=True, window=0,
                    dtype="bf16", direction="bwd"),
+    "bwd_d64": dict(name="bf16 bwd B=1 H=32 N=16384 d=64 non-causal", B=1, H=32, N=16384, d=64, causal=False,
+                    window=0, dtype="bf16", direction="bwd"),
     # The pages' FP8 figure: d = 256, 16k tokens with hidden 2048 (8 heads), N = 16k.
     "fp8_d256": dict(name="fp8 e4m3 fwd B=1 H=8 N=16384 d=256 non-causal, outliers, block scales + Hadamard", B=1, H=8,
                      N=16384, d=256, causal=False, window=0, dtype="fp8"),
@@ -103,10 +106,11 @@ def workload(spec: str) -> dict:
         return dict(name=f"bf16 fwd sweep point N={n} d={d} {'causal' if c else 'non-causal'} (16384 tokens, "
                          f"hidden 2048)", B=16384 // n, H=2048 // d, N=n, d=d, causal=c, window=0, dtype="bf16")
     if spec.startswith("bwd:"):
-        _, n, c = spec.split(":")
-        n, c = int(n), c in ("1", "true", "causal")
-        return dict(name=f"bf16 bwd sweep point N={n} d=128 {'causal' if c else 'non-causal'} (16384 tokens, "
-                         f"hidden 2048)", B=16384 // n, H=16, N=n, d=128, causal=c, window=0, dtype="bf16",
+        parts = spec.split(":")
+        n, c = int(parts[1]), parts[2] in ("1", "true", "causal")
+        d = int(parts[3]) if len(parts) > 3 else 128
+        return dict(name=f"bf16 bwd sweep point N={n} d={d} {'causal' if c else 'non-causal'} (16384 tokens, "
+                         f"hidden 2048)", B=16384 // n, H=2048 // d, N=n, d=d, causal=c, window=0, dtype="bf16",
                     direction="bwd")
     raise SystemExit(f"unknown workload {spec}")
 

@@ -342,7 +342,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     g_err[0] = '\0';
     int rc = check_common(q, k, v, o, lse, B, H, N, d, window);
     if (rc != ATTN_OK) return rc;
-    if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_bwd supports head_dim 128 only (got %d)", d);
+    if (d != 128 && d != 64) return fail(ATTN_ERR_UNSUPPORTED, "attn_bwd supports head_dim 64 and 128 (got %d)", d);
     if (H_kv <= 0 || H % H_kv != 0)
         return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
     if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
@@ -356,8 +356,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
         return fail(ATTN_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %lld bytes needed",
                     workspace_bytes, ws.bytes);
     attn::BwdMaps maps;
-    if ((rc = make_map(&maps.q, q, B, H, N, d, 2, 64)) != ATTN_OK) return rc;
-    if ((rc = make_map(&maps.dout, dout, B, H, N, d, 2, 64)) != ATTN_OK) return rc;
+    const int qrows = attn::bwd_query_rows(d);
+    if ((rc = make_map(&maps.q, q, B, H, N, d, 2, qrows)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.dout, dout, B, H, N, d, 2, qrows)) != ATTN_OK) return rc;
     if ((rc = make_map(&maps.k, k, B, H_kv, N, d, 2, 128)) != ATTN_OK) return rc;
     if ((rc = make_map(&maps.v, v, B, H_kv, N, d, 2, 128)) != ATTN_OK) return rc;
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
@@ -380,7 +381,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     p.n_kblocks = (N + 127) / 128;
     p.wait_limit = g_wait_limit.load();
     if ((rc = status_ptr(&p.status)) != ATTN_OK) return rc;
-    cudaError_t e = attn::run_bwd_d128(maps, p, o, dout, lse, dq, static_cast<cudaStream_t>(stream));
+    cudaError_t e = attn::run_bwd(d, maps, p, o, dout, lse, dq, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd launch");
     return ATTN_OK;
 }
@@ -459,7 +460,7 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      int window, void* stream) {
     g_err[0] = '\0';
     if (B < 0 || H < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d N=%d)", B, H, N);
-    if (d == 128 && static_cast<long long>(B) * H * N > 0) {
+    if ((d == 128 || d == 64) && static_cast<long long>(B) * H * N > 0) {
         const size_t need = attn_bwd_workspace_size(B, H, N, d);
         if (need > kNoAllocScratchBytes)
             return fail(ATTN_ERR_INVALID_ARG,

@@ -18,20 +18,30 @@
 namespace attn {
 namespace {
 
-// One warp per row of (B, H, N_pad); lane l holds elements [4l, 4l + 4).
+template <int E> struct Bf16Vec;
+template <> struct Bf16Vec<2> { using T = uint32_t; };
+template <> struct Bf16Vec<4> { using T = uint2; };
+
+// One warp per row of (B, H, N_pad); lane l holds elements [E l, E l + E), E = D / 32.
+template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dout,
                                                        const float* __restrict__ lse, float* __restrict__ lse2,
                                                        float* __restrict__ dvec, float* __restrict__ dq_acc, int B,
                                                        int H, int N, int N_pad) {
-    constexpr int D = 128;
+    constexpr int E = D / 32;
+    using V = typename Bf16Vec<E>::T;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= static_cast<long long>(B) * H * N_pad) return;
     const int n = static_cast<int>(row % N_pad);
     const long long bh = row / N_pad;
     const int b = static_cast<int>(bh / H), h = static_cast<int>(bh % H);
-    reinterpret_cast<float4*>(dq_acc + row * D)[lane] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if constexpr (E == 4) {
+        reinterpret_cast<float4*>(dq_acc + row * D)[lane] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    } else {
+        reinterpret_cast<float2*>(dq_acc + row * D)[lane] = make_float2(0.0f, 0.0f);
+    }
     if (n >= N) {
         if (lane == 0) {
             dvec[row] = 0.0f;
@@ -39,14 +49,14 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
         }
         return;
     }
-    const size_t off = ((static_cast<size_t>(b) * N + n) * H + h) * D + lane * 4;
-    const uint2 ov = __ldg(reinterpret_cast<const uint2*>(o + off));
-    const uint2 dv = __ldg(reinterpret_cast<const uint2*>(dout + off));
+    const size_t off = ((static_cast<size_t>(b) * N + n) * H + h) * D + lane * E;
+    const V ov = __ldg(reinterpret_cast<const V*>(o + off));
+    const V dv = __ldg(reinterpret_cast<const V*>(dout + off));
     const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
     const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
     float acc = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < E / 2; ++k) {
         const float2 a = __bfloat1622float2(o2[k]);
         const float2 c = __bfloat1622float2(d2[k]);
         acc = fmaf(a.x, c.x, acc);
@@ -60,23 +70,24 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
     }
 }
 
-// One warp per query row: dq (B, N, H, 128) bf16 = scale * dq_acc (B, H, N_pad, 128).
+// One warp per query row: dq (B, N, H, D) bf16 = scale * dq_acc (B, H, N_pad, D).
+template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq,
                                                      int B, int H, int N, int N_pad, float scale) {
-    constexpr int D = 128;
+    constexpr int E = D / 32;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= static_cast<long long>(B) * N * H) return;
     const int h = static_cast<int>(row % H);
     const long long bn = row / H;
     const int n = static_cast<int>(bn % N), b = static_cast<int>(bn / N);
-    const float4 a = __ldg(reinterpret_cast<const float4*>(dq_acc + ((static_cast<size_t>(b) * H + h) * N_pad + n) * D) + lane);
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
-    uint2 v;
-    v.x = *reinterpret_cast<uint32_t*>(&lo);
-    v.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(dq + row * D)[lane] = v;
+    const float* src = dq_acc + ((static_cast<size_t>(b) * H + h) * N_pad + n) * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+        const float2 a = __ldg(reinterpret_cast<const float2*>(src + e));
+        const __nv_bfloat162 v = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+        *reinterpret_cast<__nv_bfloat162*>(dq + row * D + lane * E + e) = v;
+    }
 }
 
 }  // namespace
@@ -94,15 +105,16 @@ BwdWorkspace bwd_workspace(int B, int H, int N, int d) {
     return ws;
 }
 
-cudaError_t run_bwd_d128(const BwdMaps& maps, const BwdParams& p, const void* o, const void* dout, const float* lse,
+template <int D>
+cudaError_t run_bwd_impl(const BwdMaps& maps, const BwdParams& p, const void* o, const void* dout, const float* lse,
                          void* dq, cudaStream_t stream) {
-    using Cfg = BwdCfg<128>;
+    using Cfg = BwdCfg<D>;
     const long long rows_pad = static_cast<long long>(p.B) * p.H * p.N_pad;
     const long long prep_blocks = (rows_pad + 7) / 8;
     const long long dq_blocks = (static_cast<long long>(p.B) * p.N * p.H + 7) / 8;
     const long long ctas = static_cast<long long>(p.n_kblocks) * p.B * p.H_kv;
     if (prep_blocks >= (1ll << 31) || dq_blocks >= (1ll << 31) || ctas >= (1ll << 31)) return cudaErrorInvalidValue;
-    bwd_prep_kernel<<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+    bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse,
         const_cast<float*>(p.lse2), const_cast<float*>(p.dvec), p.dq_acc, p.B, p.H, p.N, p.N_pad);
     cudaError_t e = cudaGetLastError();
@@ -114,9 +126,20 @@ cudaError_t run_bwd_d128(const BwdMaps& maps, const BwdParams& p, const void* o,
                                                                                    p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<<<static_cast<unsigned>(dq_blocks), 256, 0, stream>>>(p.dq_acc, static_cast<__nv_bfloat16*>(dq), p.B,
-                                                                        p.H, p.N, p.N_pad, p.scale);
+    bwd_dq_kernel<D><<<static_cast<unsigned>(dq_blocks), 256, 0, stream>>>(p.dq_acc, static_cast<__nv_bfloat16*>(dq),
+                                                                           p.B, p.H, p.N, p.N_pad, p.scale);
     return cudaGetLastError();
 }
+
+cudaError_t run_bwd(int d, const BwdMaps& maps, const BwdParams& p, const void* o, const void* dout, const float* lse,
+                    void* dq, cudaStream_t stream) {
+    switch (d) {
+        case 64: return run_bwd_impl<64>(maps, p, o, dout, lse, dq, stream);
+        case 128: return run_bwd_impl<128>(maps, p, o, dout, lse, dq, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int bwd_query_rows(int d) { return d == 128 ? BwdCfg<128>::BM : BwdCfg<64>::BM; }
 
 }  // namespace attn

@@ -23,7 +23,11 @@ struct BwdWorkspace {
 
 BwdWorkspace bwd_workspace(int B, int H, int N, int d);
 
-cudaError_t run_bwd_d128(const BwdMaps& maps, const BwdParams& p, const void* o, const void* dout, const float* lse,
-                         void* dq, cudaStream_t stream);
+// d = 64 or 128.
+cudaError_t run_bwd(int d, const BwdMaps& maps, const BwdParams& p, const void* o, const void* dout, const float* lse,
+                    void* dq, cudaStream_t stream);
+
+// Query rows per step of the fused kernel (the Q / dO tensor-map box height).
+int bwd_query_rows(int d);
 
 }  // namespace attn

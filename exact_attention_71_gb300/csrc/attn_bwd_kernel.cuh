@@ -87,19 +87,36 @@ enum : int {
 template <int D_>
 struct BwdCfg {
     static constexpr int D = D_;
-    static constexpr int BM = 64;                         // query rows per step
+    // d = 128: 64 query rows per step, S^T double-buffered, dQ computed
+    // transposed (dQ^T = K^T dS^T, head dimensions on the TMEM lanes).
+    // d = 64: 128 query rows per step (full-rate N = 128 products), one S^T
+    // buffer, dQ = dS K with the queries on the lanes (an M = 64 product is
+    // avoided).
+    static constexpr bool DQ_T = D == 128;
+    static constexpr int BM = D == 128 ? 64 : 128;        // query rows per step
+    static constexpr int S_BUFS = D == 128 ? 2 : 1;
     static constexpr int BN = 128;                        // keys per CTA
     static constexpr int NCB = D * 2 / 128;               // 128-byte column boxes per row
     static constexpr int Q_TILE = BM * D * 2;
     static constexpr int KV_TILE = BN * D * 2;
     static constexpr int NST = 2;                         // Q / dO ring depth
     static constexpr int STAGE = 2 * Q_TILE;              // Q, dO
-    static constexpr int DS_BYTES = BN * BM * 2;          // dS^T, one 128-byte row per key (x2 buffers)
-    static constexpr int DQ_STAGE = BM * D * 4;           // float32 dQ tile
+    // dS^T (x2 buffers): rows = keys, BM queries each, in 128-byte column
+    // chunks of 64 queries ([chunk][key][64 queries], 128-byte swizzle).
+    static constexpr int DS_BYTES = BN * BM * 2;
+    static constexpr int DS_CHUNK = BN * 128;             // bytes of one 64-query chunk
+    // float32 dQ staging: d = 128, [query][dim] for one bulk add per step
+    // (x2 buffers); d = 64, one row per thread padded by 16 bytes (fewer bank
+    // conflicts), one bulk add per row.
+    static constexpr int DQ_ROW = DQ_T ? D * 4 : D * 4 + 16;
+    static constexpr int DQ_STAGE = BM * DQ_ROW;
+    static constexpr int DQ_BUFS = DQ_T ? 2 : 1;
     static constexpr int VEC_BYTES = 2 * BM * 4;          // LSE2 and D of one step
-    static constexpr int DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + 2 * BM, DQ_COL = 2 * D + 3 * BM;
+    static constexpr int DV_COL = 0, DK_COL = D, S_COL = 2 * D, DP_COL = 2 * D + S_BUFS * BM,
+                         DQ_COL = 2 * D + (S_BUFS + 1) * BM;
+    static constexpr int DQ_COLS = DQ_T ? BM : D;         // TMEM columns of dQ^T / dQ
     static constexpr int TMEM_COLS = 512;
-    // Two elementwise warpgroups, each owning 32 of the 64 query columns.
+    // Two elementwise warpgroups, each owning half of the step's query columns.
     static constexpr int EW_WGS = 2, EW_COLS = BM / EW_WGS;
     static constexpr int EW_WARP0 = 0, DQ_WARP0 = 4 * EW_WGS, LOAD_WARP = DQ_WARP0 + 4, MMA_WARP = LOAD_WARP + 1;
     static constexpr int THREADS = (MMA_WARP + 1) * 32;
@@ -110,12 +127,12 @@ struct BwdCfg {
     static constexpr int OFF_STAGE = OFF_V + KV_TILE;
     static constexpr int OFF_DS = OFF_STAGE + NST * STAGE;
     static constexpr int OFF_DQ = OFF_DS + 2 * DS_BYTES;
-    static constexpr int OFF_VEC = OFF_DQ + 2 * DQ_STAGE;
+    static constexpr int OFF_VEC = OFF_DQ + DQ_BUFS * DQ_STAGE;
     static constexpr int OFF_BAR = OFF_VEC + NST * VEC_BYTES;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + BAR_BYTES;
 
-    static_assert(D == 128, "the backward is built for head_dim 128");
-    static_assert(DQ_COL + BM <= TMEM_COLS, "tensor memory budget");
+    static_assert(D == 128 || D == 64, "the backward is built for head_dim 64 and 128");
+    static_assert(DQ_COL + DQ_COLS <= TMEM_COLS, "tensor memory budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -308,13 +325,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aDS = smem_u32(sDS);
             const uint64_t k_kmaj = sdesc_sw128(aK, 16, 1024);
             const uint64_t v_kmaj = sdesc_sw128(aV, 16, 1024);
-            const uint64_t k_mn = sdesc_sw128(aK, BN * 128, 1024);          // K^T as the A operand of dQ^T
+            const uint64_t k_mn = sdesc_sw128(aK, BN * 128, 1024);          // K read MN-major (dQ^T: A; dQ: B)
 
             constexpr uint32_t id_s = make_idesc_ab(1, 128, BM, 0, 0);      // S^T, dP^T
             constexpr uint32_t id_acc = make_idesc_ab(1, 128, D, 0, 1);     // dV, dK (B MN-major)
-            // dS^T buffer of step t: rows = keys, 64 queries (128 bytes) each.
+            // dS^T buffer of step t: rows = keys, BM queries each (64-query chunks).
             auto ds_addr = [&](int t) { return aDS + (t & 1) * Cfg::DS_BYTES; };
-            constexpr uint32_t id_dq = make_idesc_ab(1, D, BM, 1, 1);       // dQ^T (A, B MN-major)
+            // dQ^T = K^T dS^T (M = d) or dQ = dS K (M = BM); both operands MN-major.
+            constexpr uint32_t id_dq = Cfg::DQ_T ? make_idesc_ab(1, D, BM, 1, 1) : make_idesc_ab(1, BM, D, 1, 1);
             bool ok = bwait_warp(&bars->kv_full, 0, abort_flag, p, BSITE_MMA_KV);
 
             // S^T = K Q^T or dP^T = V dO^T into `d_col`: d / 16 MMAs, both operands K-major.
@@ -329,9 +347,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             };
             // acc (+)= X^T Y with X^T (bf16 pairs) in tensor memory at x_col and
-            // Y (64 query rows x d) in shared memory, read MN-major.
-            // P^T of query columns [32 g, 32 g + 32) sits at columns
-            // [32 g, 32 g + 16) of its S^T buffer (written by warpgroup g).
+            // Y (BM query rows x d) in shared memory, read MN-major.
+            // P^T of query columns [EC g, EC g + EC) sits at columns
+            // [EC g, EC g + EC / 2) of its S^T buffer (written by warpgroup g).
             auto issue_acc = [&](uint32_t d_col, uint32_t x_col, uint32_t y_addr, bool accumulate) {
                 const uint64_t y_desc = sdesc_sw128(y_addr, BM * 128, 1024);
 #pragma unroll
@@ -349,21 +367,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tc_fence_after();
                 if (elect_one()) {
                     issue_kq(Cfg::S_COL, k_kmaj, stage_addr(0));
-                    mma_commit(&bars->s_full[0]);
+                    mma_commit(&bars->s_full[0]);   // buffer 0 for step 0 either way
                     issue_kq(Cfg::DP_COL, v_kmaj, stage_addr(0) + Cfg::Q_TILE);
                     mma_commit(&bars->dp_full);
                 }
                 __syncwarp();
             }
+            constexpr int SB = Cfg::S_BUFS;
             for (int t = 0; t < T && ok; ++t) {
                 const uint32_t sa = stage_addr(t);
-                const uint32_t s_col = Cfg::S_COL + (t & 1) * BM;
+                const uint32_t s_col = Cfg::S_COL + (t % SB) * BM;
                 // dV += P^T dO
-                if (!bwait_warp(&bars->p_full[t & 1], (t >> 1) & 1, abort_flag, p, BSITE_MMA_P)) { ok = false; break; }
+                if (!bwait_warp(&bars->p_full[t % SB], (t / SB) & 1, abort_flag, p, BSITE_MMA_P)) { ok = false; break; }
                 tc_fence_after();
                 if (elect_one()) issue_acc(Cfg::DV_COL, s_col, sa + Cfg::Q_TILE, t > 0);
                 __syncwarp();
-                // S^T of the next step into the other buffer
+                // S^T of the next step (into the other buffer when there are two;
+                // with one, after dV has been issued, which the pipe runs first)
                 if (t + 1 < T) {
                     if (!bwait_warp(&bars->q_full[(t + 1) % NST], ((t + 1) / NST) & 1, abort_flag, p, BSITE_MMA_Q)) {
                         ok = false;
@@ -371,8 +391,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     tc_fence_after();
                     if (elect_one()) {
-                        issue_kq(Cfg::S_COL + ((t + 1) & 1) * BM, k_kmaj, stage_addr(t + 1));
-                        mma_commit(&bars->s_full[(t + 1) & 1]);
+                        issue_kq(Cfg::S_COL + ((t + 1) % SB) * BM, k_kmaj, stage_addr(t + 1));
+                        mma_commit(&bars->s_full[(t + 1) % SB]);
                     }
                     __syncwarp();
                 }
@@ -388,18 +408,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint64_t ds_k = sdesc_sw128(ds_addr(t), 16, 1024);
                     const uint64_t q_mn = sdesc_sw128(sa, BM * 128, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BM / 16; ++kk)
-                        mma_f16_ss(tmem + Cfg::DK_COL, ds_k + ((kk * 32) >> 4), q_mn + ((kk * 16 * 128) >> 4), id_acc,
+                    for (int kk = 0; kk < BM / 16; ++kk) {
+                        const uint32_t a_off = ((kk * 32) / 128) * Cfg::DS_CHUNK + (kk * 32) % 128;
+                        mma_f16_ss(tmem + Cfg::DK_COL, ds_k + (a_off >> 4), q_mn + ((kk * 16 * 128) >> 4), id_acc,
                                    (t > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 __syncwarp();
                 if (!bwait_warp(&bars->dq_empty, (t & 1) ^ 1, abort_flag, p, BSITE_MMA_DQ)) { ok = false; break; }
                 tc_fence_after();
                 if (elect_one()) {
-                    const uint64_t ds_mn = sdesc_sw128(ds_addr(t), BN * 128, 1024);
+                    const uint64_t ds_mn = sdesc_sw128(ds_addr(t), Cfg::DS_CHUNK, 1024);
+                    const uint64_t a_dq = Cfg::DQ_T ? k_mn : ds_mn, b_dq = Cfg::DQ_T ? ds_mn : k_mn;
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_f16_ss(tmem + Cfg::DQ_COL, k_mn + ((kk * 16 * 128) >> 4), ds_mn + ((kk * 16 * 128) >> 4),
+                        mma_f16_ss(tmem + Cfg::DQ_COL, a_dq + ((kk * 16 * 128) >> 4), b_dq + ((kk * 16 * 128) >> 4),
                                    id_dq, kk > 0 ? 1u : 0u);
                     mma_commit(&bars->dq_full);
                     // Q_t and dO_t are no longer read by any MMA.
@@ -424,74 +447,80 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int key = w.k0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         bool ok = true;
+        constexpr int SB = Cfg::S_BUFS;
         for (int t = 0; t < T && ok; ++t) {
             const int st = t % NST;
             const int q0 = w.q0(t, BM) + g * EC;
-            const uint32_t s_tm = tmem + lane_off + Cfg::S_COL + (t & 1) * BM + g * EC;
+            const uint32_t s_tm = tmem + lane_off + Cfg::S_COL + (t % SB) * BM + g * EC;
             const uint32_t dp_tm = tmem + lane_off + Cfg::DP_COL + g * EC;
             if (!bwait_warp(&bars->q_full[st], (t / NST) & 1, abort_flag, p, BSITE_EW_Q)) { ok = false; break; }
-            if (!bwait_warp(&bars->s_full[t & 1], (t >> 1) & 1, abort_flag, p, BSITE_EW_S)) { ok = false; break; }
+            if (!bwait_warp(&bars->s_full[t % SB], (t / SB) & 1, abort_flag, p, BSITE_EW_S)) { ok = false; break; }
             tc_fence_after();
             const float* lse2 = sVec + st * (2 * BM) + g * EC;
-            const float* dvec = lse2 + BM;
+            const float* dvec = sVec + st * (2 * BM) + BM + g * EC;
             // Visible queries of this key: [qlo, qhi].
             const int qlo = p.causal ? key : 0;
             const int qhi = p.window > 0 ? key + p.window - 1 : 0x7fffffff;
             const bool key_ok = key < p.N;
             const bool full = key_ok && q0 >= qlo && q0 + EC - 1 <= qhi;
             float pr[EC];
-            {
-                uint32_t sr[EC];
-                tmem_ld32(s_tm, sr);
+            // 32 columns at a time: read S^T, then write P^T (bf16 pairs) over
+            // the first half of this warpgroup's own S^T columns -- the part
+            // already read -- so the two warpgroups never overwrite each
+            // other's scores.
+#pragma unroll
+            for (int c = 0; c < EC / 32; ++c) {
+                uint32_t sr[32];
+                tmem_ld32(s_tm + c * 32, sr);
                 tmem_wait_ld();
                 reg_fence32(sr);
-                uint32_t pk[EC / 2];
+                uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < EC; ++x) {
-                    float v = ex2_approx(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[x]));
+                for (int x = 0; x < 32; ++x) {
+                    const int qi = c * 32 + x;
+                    float v = ex2_approx(fmaf(__uint_as_float(sr[x]), p.scale_log2, -lse2[qi]));
                     if (!full) {
-                        const int q = q0 + x;
+                        const int q = q0 + qi;
                         if (!key_ok || q < qlo || q > qhi) v = 0.0f;
                     }
-                    pr[x] = v;
+                    pr[qi] = v;
                 }
 #pragma unroll
-                for (int x = 0; x < EC / 2; ++x) pk[x] = pack_bf16x2(pr[2 * x], pr[2 * x + 1]);
-                // P^T over the first half of this warpgroup's own S^T columns
-                // (read above), so the two warpgroups never overwrite each
-                // other's scores.
-                tmem_st16(s_tm, pk);
+                for (int x = 0; x < 16; ++x) pk[x] = pack_bf16x2(pr[c * 32 + 2 * x], pr[c * 32 + 2 * x + 1]);
+                tmem_st16(s_tm + c * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars->p_full[t & 1]);
+            mbar_arrive(&bars->p_full[t % SB]);
 
             if (!bwait_warp(&bars->dp_full, t & 1, abort_flag, p, BSITE_EW_DP)) { ok = false; break; }
             tc_fence_after();
             // dS^T(t) goes to buffer t & 1; the MMAs of step t - 2 that read
             // it were issued before dP^T(t), whose completion this thread has
             // just observed.
-            uint8_t* ds_row = sDS + (t & 1) * Cfg::DS_BYTES + r * 128;
-            {
-                uint32_t dr[EC];
-                tmem_ld32(dp_tm, dr);
+            uint8_t* ds_buf = sDS + (t & 1) * Cfg::DS_BYTES;
+#pragma unroll
+            for (int c = 0; c < EC / 32; ++c) {
+                uint32_t dr[32];
+                tmem_ld32(dp_tm + c * 32, dr);
                 tmem_wait_ld();
                 reg_fence32(dr);
-                uint32_t pk[EC / 2];
+                uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < EC / 2; ++x) {
-                    const float d0 = pr[2 * x] * (__uint_as_float(dr[2 * x]) - dvec[2 * x]);
-                    const float d1 = pr[2 * x + 1] * (__uint_as_float(dr[2 * x + 1]) - dvec[2 * x + 1]);
+                for (int x = 0; x < 16; ++x) {
+                    const int qi = c * 32 + 2 * x;
+                    const float d0 = pr[qi] * (__uint_as_float(dr[2 * x]) - dvec[qi]);
+                    const float d1 = pr[qi + 1] * (__uint_as_float(dr[2 * x + 1]) - dvec[qi + 1]);
                     pk[x] = pack_bf16x2(d0, d1);
                 }
-                // dS^T row of this key into shared memory (128-byte swizzle:
-                // 16-byte chunk j of row r sits at chunk j ^ (r % 8)); this
-                // warpgroup owns chunks [4 g, 4 g + 4).
+                // dS^T row of this key into shared memory: 16-byte piece j of
+                // the row sits in 64-query chunk j / 8 at position
+                // (j % 8) ^ (key % 8) (128-byte swizzle).
 #pragma unroll
                 for (int y = 0; y < 4; ++y) {
-                    const int chunk = (g * 4 + y) ^ (r & 7);
-                    *reinterpret_cast<uint4*>(ds_row + chunk * 16) =
-                        make_uint4(pk[4 * y], pk[4 * y + 1], pk[4 * y + 2], pk[4 * y + 3]);
+                    const int piece = (g * EC + c * 32) / 8 + y;
+                    uint8_t* dst = ds_buf + (piece / 8) * Cfg::DS_CHUNK + r * 128 + (((piece % 8) ^ (r & 7)) * 16);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * y], pk[4 * y + 1], pk[4 * y + 2], pk[4 * y + 3]);
                 }
             }
             fence_proxy_async_smem();
@@ -534,42 +563,72 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else {
         // ------------------------------------------------------------ dQ: tensor memory -> bulk add
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;                  // head dimension (dQ^T) / key row (dK)
+        const int r = quad * 32 + lane;                  // dimension (dQ^T) or query (dQ); key row (dK)
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         const bool leader = threadIdx.x == Cfg::DQ_WARP0 * 32;
         bool ok = true;
         for (int t = 0; t < T && ok; ++t) {
             const int h = w.head(t, p.group);
             const int q0 = w.q0(t, BM);
-            const bool got = bwait_warp(&bars->dq_full, t & 1, abort_flag, p, BSITE_DQ_FULL);
-            // The staging buffer of this step was last read by the bulk add of
-            // step t - 2; at most one (step t - 1's) may still be reading.
-            if (leader) bulk_wait_group_read<1>();
-            // One decision for the four warps (a warp that gave up must not
-            // leave the others waiting at the barriers below); the barrier
-            // also tells everyone that the staging buffer is free.
-            if (!named_barrier_and(1, 128, got)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t a[BM];
+            if constexpr (Cfg::DQ_T) {
+                // dQ^T: thread = head dimension r, BM query values.
+                const bool got = bwait_warp(&bars->dq_full, t & 1, abort_flag, p, BSITE_DQ_FULL);
+                // The staging buffer of this step was last read by the bulk add of
+                // step t - 2; at most one (step t - 1's) may still be reading.
+                if (leader) bulk_wait_group_read<1>();
+                // One decision for the four warps (a warp that gave up must not
+                // leave the others waiting at the barriers below); the barrier
+                // also tells everyone that the staging buffer is free.
+                if (!named_barrier_and(1, 128, got)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t a[BM];
 #pragma unroll
-            for (int c = 0; c < BM / 32; ++c) tmem_ld32(tmem + lane_off + Cfg::DQ_COL + c * 32, a + c * 32);
-            tmem_wait_ld();
+                for (int c = 0; c < BM / 32; ++c) tmem_ld32(tmem + lane_off + Cfg::DQ_COL + c * 32, a + c * 32);
+                tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < BM / 32; ++c) reg_fence32(a + c * 32);
-            tc_fence_before();
-            mbar_arrive(&bars->dq_empty);
-            float* stage = reinterpret_cast<float*>(sDQ + (t & 1) * Cfg::DQ_STAGE);
+                for (int c = 0; c < BM / 32; ++c) reg_fence32(a + c * 32);
+                tc_fence_before();
+                mbar_arrive(&bars->dq_empty);
+                float* stage = reinterpret_cast<float*>(sDQ + (t & 1) * Cfg::DQ_STAGE);
 #pragma unroll
-            for (int x = 0; x < BM; ++x) stage[x * D + r] = __uint_as_float(a[x]);
-            fence_proxy_async_smem();
-            named_barrier(1, 128);
-            if (leader) {
-                float* dst = p.dq_acc + ((static_cast<size_t>(w.b) * p.H + h) * p.N_pad + q0) * D;
-                bulk_reduce_add_f32(dst, stage, Cfg::DQ_STAGE);
-                bulk_commit_group();
+                for (int x = 0; x < BM; ++x) stage[x * D + r] = __uint_as_float(a[x]);
+                fence_proxy_async_smem();
+                named_barrier(1, 128);
+                if (leader) {
+                    float* dst = p.dq_acc + ((static_cast<size_t>(w.b) * p.H + h) * p.N_pad + q0) * D;
+                    bulk_reduce_add_f32(dst, stage, Cfg::DQ_STAGE);
+                    bulk_commit_group();
+                }
+            } else {
+                // dQ: thread = query row r of the step, d values.  Each thread
+                // stages its own row (padded rows: the warp's 16-byte stores
+                // spread over the banks) and adds it with its own bulk add, so
+                // the four warps need no barrier between them.
+                if (!bwait_warp(&bars->dq_full, t & 1, abort_flag, p, BSITE_DQ_FULL)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t a[D];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) tmem_ld32(tmem + lane_off + Cfg::DQ_COL + c * 32, a + c * 32);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) reg_fence32(a + c * 32);
+                tc_fence_before();
+                mbar_arrive(&bars->dq_empty);
+                // This thread's previous bulk add has finished reading its row.
+                bulk_wait_group_read<0>();
+                uint8_t* row = sDQ + r * Cfg::DQ_ROW;
+#pragma unroll
+                for (int x = 0; x < D / 4; ++x)
+                    *reinterpret_cast<uint4*>(row + x * 16) = make_uint4(a[4 * x], a[4 * x + 1], a[4 * x + 2], a[4 * x + 3]);
+                fence_proxy_async_smem();
+                if (q0 + r < p.N_pad) {
+                    float* dst = p.dq_acc + ((static_cast<size_t>(w.b) * p.H + h) * p.N_pad + q0 + r) * D;
+                    bulk_reduce_add_f32(dst, row, D * 4);
+                    bulk_commit_group();
+                }
             }
         }
-        if (leader) bulk_wait_group_all();
+        if (Cfg::DQ_T ? leader : true) bulk_wait_group_all();
         // dK epilogue: thread = key row, scaled by the softmax scale.
         if (ok && T > 0) ok = bwait_warp(&bars->acc_full, 0, abort_flag, p, BSITE_DQ_ACC);
         if (ok || T == 0) {

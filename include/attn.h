@@ -196,7 +196,7 @@ int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float*
  *                         so calls sharing one workspace must be ordered on
  *                         one stream)
  *   B, H, H_kv, N, d, causal, scale, window : as attn_fwd_gqa
- * Only d = 128 is supported (ATTN_ERR_UNSUPPORTED otherwise).  Three
+ * d must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise).  Three
  * launches on `stream`: D and the zeroed float32 dQ accumulator, the fused
  * backward, and the conversion of dQ to bf16.  Errors: as attn_fwd_gqa; a
  * NULL, unaligned or too small workspace is ATTN_ERR_INVALID_ARG.

@@ -107,7 +107,7 @@ def test_backward_arguments_checked(lib):
     assert lib.attn_bwd_workspace_size(-1, 2, 100, 128) == 0
     args = lambda d=128, hkv=2, wsp=FAKE, wsb=ws: (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, wsp, wsb,
                                                    1, 2, hkv, 100, d, 1, 0.0, 0, None)
-    assert f(*args(d=64)) == -2
+    assert f(*args(d=256)) == -2
     assert f(*args(hkv=3)) == -1
     assert f(*args(wsp=None)) == -1
     assert f(*args(wsp=ctypes.c_void_p((1 << 20) + 16))) == -1

@@ -56,23 +56,36 @@ def _check(got, ref, label):
         assert a <= REL_RMS and b <= REL_MAX, (label, name, a, b)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [64, 129, 300, 1000])
 @pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 97), (False, 200)])
-def test_backward_matches_oracle(N, causal, window):
-    B, H, d = 1, 2, 128
+def test_backward_matches_oracle(N, causal, window, d):
+    B, H = 1, 2
     q, k, v, do = _inputs(B, N, H, d, seed=N)
     got = _gpu_grads(q, k, v, do, causal, window)
     ref = oracle.attention_bwd(q, k, v, do, causal=causal, window=window)
-    _check(got, ref, f"N={N} causal={causal} W={window}")
+    _check(got, ref, f"d={d} N={N} causal={causal} W={window}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("Hkv", [1, 2])
-def test_backward_grouped_query(Hkv):
-    B, N, H, d = 2, 257, 4, 128
+def test_backward_grouped_query(Hkv, d):
+    B, N, H = 2, 257, 4
     q, k, v, do = _inputs(B, N, H, d, Hkv=Hkv, seed=7)
     got = _gpu_grads(q, k, v, do, True, 0)
     ref = oracle.attention_bwd(q, k, v, do, causal=True)
-    _check(got, ref, f"GQA H={H} Hkv={Hkv}")
+    _check(got, ref, f"GQA d={d} H={H} Hkv={Hkv}")
+
+
+def test_backward_head_dim_64_full_size_heads():
+    """B=1, H=32, N=8192, d=64, causal: two heads against the oracle."""
+    B, N, H, d = 1, 8192, 32, 64
+    q, k, v, do = _inputs(B, N, H, d, seed=5)
+    dq, dk, dv = _gpu_grads(q, k, v, do, True, 0)
+    for h in (0, 17):
+        sl = slice(h, h + 1)
+        ref = oracle.attention_bwd(q[:, :, sl], k[:, :, sl], v[:, :, sl], do[:, :, sl], causal=True)
+        _check([dq[:, :, sl], dk[:, :, sl], dv[:, :, sl]], ref, f"d=64 N=8192 head {h}")
 
 
 def test_backward_full_size_heads_and_invariants():
