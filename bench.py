@@ -11,7 +11,8 @@ pages' Fig. 6 point (B=1, H=16, N=16384, d=128, non-causal; FLOPs 2.5 x the
 forward's) in its "bwd" object.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c2|c4|c5|gqa|bwd|bwd_c2|bwd_d64|sparse|fp8_d256|c3:N:d:causal|bwd:N:causal[:d]]
+                    [--workload c2|c4|c5|gqa|bwd|bwd_c2|bwd_d64|sparse|fp8_d256|c3:N:d:causal|fp8:N:d:causal|
+                                bwd:N:causal[:d]]
                     [--quick]
 
 Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
@@ -105,6 +106,12 @@ def workload(spec: str) -> dict:
         n, d, c = int(n), int(d), c in ("1", "true", "causal")
         return dict(name=f"bf16 fwd sweep point N={n} d={d} {'causal' if c else 'non-causal'} (16384 tokens, "
                          f"hidden 2048)", B=16384 // n, H=2048 // d, N=n, d=d, causal=c, window=0, dtype="bf16")
+    if spec.startswith("fp8:"):
+        _, n, d, c = spec.split(":")
+        n, d, c = int(n), int(d), c in ("1", "true", "causal")
+        return dict(name=f"fp8 e4m3 fwd sweep point N={n} d={d} {'causal' if c else 'non-causal'} (16384 tokens, "
+                         f"hidden 2048), outliers, block scales + Hadamard", B=16384 // n, H=2048 // d, N=n, d=d,
+                    causal=c, window=0, dtype="fp8")
     if spec.startswith("bwd:"):
         parts = spec.split(":")
         n, c = int(parts[1]), parts[2] in ("1", "true", "causal")
@@ -163,6 +170,7 @@ KERNEL_SOURCES = {
     "attn_fwd": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_bf16_d128.cu"),
     "attn_fwd_fp8": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d128.cu"),
     "attn_fwd_fp8_d256": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d256.cu"),
+    "attn_fwd_fp8_d64": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d64.cu"),
     "fp8_prep": ("fp8_prep.cu", "fp8_prep.cuh"),
     "attn_bwd": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_bwd_kernel.cuh", "attn_bwd.cu", "attn_bwd.cuh"),
     "attn_fwd_sparse": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_sparse_d128.cu"),
@@ -578,7 +586,7 @@ def main():
     value = ws * flops * args.steps / (ms_total / 1e3) / 1e12
     peaks, peak_src = load_peaks()
     achieved = flops / (ms_step / 1e3) / 1e12
-    kernel = ("attn_fwd_fp8" + ("_d256" if w["d"] == 256 else "")) if w["dtype"] == "fp8" else (
+    kernel = ("attn_fwd_fp8" + {128: "", 256: "_d256", 64: "_d64"}[w["d"]]) if w["dtype"] == "fp8" else (
         "attn_bwd" if bwd else ("attn_fwd_sparse" if w.get("sparse") else "attn_fwd"))
     if w["dtype"] == "fp8":
         fp8_peak = peaks.get("fp8_tflops") or 2.0 * peaks["bf16_tflops"]

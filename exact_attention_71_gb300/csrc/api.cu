@@ -94,10 +94,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// (B, N, H, d) tensor viewed as 4-D {d, H, N, B}; box = one 128-byte column
-// block of `rows` tokens of one head, 128-byte swizzle (the layout the MMA
-// shared-memory descriptors expect).  Rows past N read as zero.
-int make_map(CUtensorMap* map, const void* base, int B, int H, int N, int d, int elem_bytes, int rows) {
+// (B, N, H, d) tensor viewed as 4-D {d, H, N, B}; box = one `swizzle`-byte
+// column block (128, or 64 for 64-byte rows) of `rows` tokens of one head,
+// with that swizzle (the layout the MMA shared-memory descriptors expect).
+// Rows past N read as zero.
+int make_map(CUtensorMap* map, const void* base, int B, int H, int N, int d, int elem_bytes, int rows,
+             int swizzle = 128) {
     auto enc = encode_fn();
     if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const CUtensorMapDataType dt =
@@ -106,10 +108,11 @@ int make_map(CUtensorMap* map, const void* base, int B, int H, int N, int d, int
                           static_cast<cuuint64_t>(B)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * elem_bytes, static_cast<cuuint64_t>(H) * d * elem_bytes,
                              static_cast<cuuint64_t>(N) * H * d * elem_bytes};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elem_bytes), 1, static_cast<cuuint32_t>(rows), 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(swizzle / elem_bytes), 1, static_cast<cuuint32_t>(rows), 1};
     cuuint32_t estride[4] = {1, 1, 1, 1};
     CUresult r = enc(map, dt, 4, const_cast<void*>(base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
     return ATTN_OK;
@@ -184,11 +187,14 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
         if (d == 128) {
             g = attn::geom_fp8_d128();
             run = attn::run_fwd_fp8_d128;
+        } else if (d == 64) {
+            g = attn::geom_fp8_d64();
+            run = attn::run_fwd_fp8_d64;
         } else if (d == 256) {
             g = attn::geom_fp8_d256();
             run = attn::run_fwd_fp8_d256;
         } else {
-            return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 and 256 (got %d)", d);
+            return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 64, 128 and 256 (got %d)", d);
         }
     } else if (d == 64) {
         g = attn::geom_bf16_d64();
@@ -202,9 +208,9 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
     }
     attn::FwdMaps maps;
     int rc;
-    if ((rc = make_map(&maps.q, q, B, H, N, d, g.elem_bytes, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(&maps.k, k, B, Hkv, N, d, g.elem_bytes, g.bn)) != ATTN_OK) return rc;
-    if ((rc = make_map(&maps.v, v, B, Hkv, N, d, g.elem_bytes, g.bn)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.q, q, B, H, N, d, g.elem_bytes, 128, g.swizzle)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.k, k, B, Hkv, N, d, g.elem_bytes, g.bn, g.swizzle)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.v, v, B, Hkv, N, d, g.elem_bytes, g.bn, g.swizzle)) != ATTN_OK) return rc;
     attn::FwdParams p{};
     p.o = o;
     p.lse = lse;
@@ -268,8 +274,8 @@ int attn_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o, fl
     if (H_kv <= 0 || H % H_kv != 0)
         return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
     if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
-    if (d != 128 && d != 256)
-        return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 128 and 256 (got %d)", d);
+    if (d != 64 && d != 128 && d != 256)
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 supports head_dim 64, 128 and 256 (got %d)", d);
     if (!q_scale || !k_scale || !v_scale) return fail(ATTN_ERR_INVALID_ARG, "null scale pointer");
     return launch_forward(true, q8, k8, v8, o, lse, B, H, H_kv, N, d, causal, scale, window, q_scale, k_scale,
                           v_scale, stream);

@@ -78,8 +78,11 @@ struct FwdCfg {
     static constexpr int BM = 128;                       // query rows per tile
     static constexpr int ES = FP8 ? 1 : 2;               // bytes per element
     static constexpr int ROW_BYTES = D * ES;
-    static constexpr int NCB = ROW_BYTES / 128;          // 128-byte column boxes
-    static constexpr int BOX_ELEMS = 128 / ES;
+    // Swizzle span: 128-byte column boxes, or one 64-byte box when a row is
+    // 64 bytes (e4m3, d = 64).  Tiles are [box][rows][SW bytes].
+    static constexpr int SW = ROW_BYTES >= 128 ? 128 : 64;
+    static constexpr int NCB = ROW_BYTES / SW;           // column boxes per row
+    static constexpr int BOX_ELEMS = SW / ES;
     static constexpr int Q_TILE_BYTES = BM * ROW_BYTES;
     static constexpr int KV_TILE_BYTES = BN * ROW_BYTES;
     // A ring stage holds what key-tile step u consumes: K_u (for S(u)) and
@@ -120,7 +123,7 @@ struct FwdCfg {
 
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
     static_assert(BN == 64 || BN == 128, "key tile");
-    static_assert(NCB >= 1 && ROW_BYTES % 128 == 0, "rows must be whole 128-byte boxes");
+    static_assert(NCB >= 1 && ROW_BYTES % SW == 0, "rows must be whole swizzle boxes");
     static_assert(NQ * 128 + 0 <= 256 && O_COL0 + NQ * D <= TMEM_COLS, "tensor memory budget");
     static_assert(NSTAGE >= 2, "ring depth");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -366,8 +369,9 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t qdesc, uint64
     for (int kk = 0; kk < Cfg::D / Cfg::MMA_K; ++kk) {
         constexpr int step_bytes = Cfg::MMA_K * Cfg::ES;
         const int byte_k = kk * step_bytes;
-        const uint32_t a_off = (byte_k / 128) * (Cfg::BM * 128) + (byte_k % 128);
-        const uint32_t b_off = (byte_k / 128) * (Cfg::BN * 128) + (byte_k % 128);
+        constexpr int SW = Cfg::SW;
+        const uint32_t a_off = (byte_k / SW) * (Cfg::BM * SW) + (byte_k % SW);
+        const uint32_t b_off = (byte_k / SW) * (Cfg::BN * SW) + (byte_k % SW);
         if constexpr (Cfg::FP8)
             mma_f8_ss(s_tmem, qdesc + (a_off >> 4), kdesc + (b_off >> 4), idesc, kk > 0 ? 1u : 0u);
         else
@@ -384,7 +388,7 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
     const uint32_t acc0 = accumulate ? 1u : 0u;
 #pragma unroll
     for (int kk = 0; kk < Cfg::BN / Cfg::MMA_K; ++kk) {
-        const uint64_t off = (static_cast<uint64_t>(kk) * Cfg::MMA_K * 128) >> 4;
+        const uint64_t off = (static_cast<uint64_t>(kk) * Cfg::MMA_K * Cfg::SW) >> 4;
         if constexpr (Cfg::FP8)
             mma_f8_ts(o_tmem, p_tmem + kk * (Cfg::MMA_K / 4), vdesc + off, idesc, kk > 0 ? 1u : acc0);
         else
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     mbar_arrive_expect_tx(&bars->q_full[t], Cfg::Q_TILE_BYTES);
 #pragma unroll
                     for (int cb = 0; cb < Cfg::NCB; ++cb)
-                        tma_load_4d(sQ + t * Cfg::Q_TILE_BYTES + cb * (BM * 128), &tmap_q, &bars->q_full[t],
+                        tma_load_4d(sQ + t * Cfg::Q_TILE_BYTES + cb * (BM * Cfg::SW), &tmap_q, &bars->q_full[t],
                                     cb * Cfg::BOX_ELEMS, w.h, w.q0 + t * BM, w.b, pol_q);
                 }
                 // Steps over the item's key tiles u (in order) and one more:
@@ -488,13 +492,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (with_k) {
 #pragma unroll
                         for (int cb = 0; cb < Cfg::NCB; ++cb)
-                            tma_load_4d(dst + cb * (BN * 128), &tmap_k, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS,
+                            tma_load_4d(dst + cb * (BN * Cfg::SW), &tmap_k, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS,
                                         w.h / p.group, u * BN, w.b, pol_kv);
                     }
                     if (with_v) {
 #pragma unroll
                         for (int cb = 0; cb < Cfg::NCB; ++cb)
-                            tma_load_4d(dst + Cfg::KV_TILE_BYTES + cb * (BN * 128), &tmap_v, &bars->ring_full[stage],
+                            tma_load_4d(dst + Cfg::KV_TILE_BYTES + cb * (BN * Cfg::SW), &tmap_v, &bars->ring_full[stage],
                                         cb * Cfg::BOX_ELEMS, w.h / p.group, prev * BN, w.b, pol_kv);
                     }
                     ++it;
@@ -531,7 +535,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         volatile int* issued = &bars->issued_blocks;
         uint64_t qdesc[NQ];
 #pragma unroll
-        for (int t = 0; t < NQ; ++t) qdesc[t] = sdesc_sw128(smem_u32(sQ) + t * Cfg::Q_TILE_BYTES, 16, 1024);
+        for (int t = 0; t < NQ; ++t)
+            qdesc[t] = sdesc_swz<Cfg::SW>(smem_u32(sQ) + t * Cfg::Q_TILE_BYTES, 16, 8 * Cfg::SW);
         uint32_t it = 0;
         uint32_t pv_count[NQ], qn[NQ];
 #pragma unroll
@@ -559,8 +564,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 }
                 const uint32_t st_addr = sKV_addr + stage * Cfg::STAGE_BYTES;
-                const uint64_t kdesc = sdesc_sw128(st_addr, 16, 1024);
-                const uint64_t vdesc = sdesc_sw128(st_addr + Cfg::KV_TILE_BYTES, BN * 128, 1024);
+                const uint64_t kdesc = sdesc_swz<Cfg::SW>(st_addr, 16, 8 * Cfg::SW);
+                const uint64_t vdesc = sdesc_swz<Cfg::SW>(st_addr + Cfg::KV_TILE_BYTES, BN * Cfg::SW, 8 * Cfg::SW);
                 bool issued_any = false;
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {

@@ -13,12 +13,12 @@ struct FwdMaps {
 
 // Tile geometry an instantiation needs from the host (tensor-map boxes).
 struct FwdGeometry {
-    int d, bn, nq, elem_bytes, threads, smem_bytes, stages;
+    int d, bn, nq, elem_bytes, threads, smem_bytes, stages, swizzle;
 };
 
 template <class Cfg>
 FwdGeometry fwd_geometry() {
-    return FwdGeometry{Cfg::D, Cfg::BN, Cfg::NQ, Cfg::ES, Cfg::THREADS, Cfg::SMEM_BYTES, Cfg::NSTAGE};
+    return FwdGeometry{Cfg::D, Cfg::BN, Cfg::NQ, Cfg::ES, Cfg::THREADS, Cfg::SMEM_BYTES, Cfg::NSTAGE, Cfg::SW};
 }
 
 template <class Cfg>
@@ -55,6 +55,8 @@ FwdGeometry geom_bf16_d256();
 FwdGeometry geom_fp8_d128();
 cudaError_t run_fwd_fp8_d256(const FwdMaps&, const FwdParams&, int, cudaStream_t);
 FwdGeometry geom_fp8_d256();
+cudaError_t run_fwd_fp8_d64(const FwdMaps&, const FwdParams&, int, cudaStream_t);
+FwdGeometry geom_fp8_d64();
 cudaError_t run_fwd_sparse_d64(const FwdMaps&, const FwdParams&, int, cudaStream_t);
 cudaError_t run_fwd_sparse_d128(const FwdMaps&, const FwdParams&, int, cudaStream_t);
 cudaError_t run_fwd_sparse_d256(const FwdMaps&, const FwdParams&, int, cudaStream_t);

@@ -186,6 +186,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// The same with the swizzle span given in bytes (128 or 64): layout type 2
+// (128-byte swizzle) or 4 (64-byte swizzle).
+template <int SW>
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    static_assert(SW == 128 || SW == 64, "swizzle span");
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(SW == 128 ? 2 : 4) << 61;
+    return d;
+}
+
 // Instruction descriptor for kind::f16 / kind::f8f6f4 (dense):
 //   [4,6) D format (1 = f32), [7,10) A format, [10,13) B format
 //   (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3),

@@ -85,7 +85,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * P8 = e4m3(P * 16 * v_scale_j / vmax) with vmax the largest V block scale
  * of the (batch, head) and P <= 16 (the row maximum used in P moves only when
  * a score exceeds it by more than 4 in log2 units); O = (sum P8 V8) * vmax /
- * (16 * l).  d must be 128 or 256 (ATTN_ERR_UNSUPPORTED otherwise).
+ * (16 * l).  d must be 64, 128 or 256 (ATTN_ERR_UNSUPPORTED otherwise).
  */
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse,
                  int B, int H, int N, int d, int causal, float scale, int window,

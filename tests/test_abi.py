@@ -63,7 +63,7 @@ def test_empty_problem_is_ok_without_launch(lib):
 
 
 def test_fp8_arguments_checked(lib):
-    assert lib.attn_fwd_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, 0, 0.0, 0, FAKE, FAKE, FAKE, None) == -2
+    assert lib.attn_fwd_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 96, 0, 0.0, 0, FAKE, FAKE, FAKE, None) == -2
     assert lib.attn_fwd_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 128, 0, 0.0, 0, None, FAKE, FAKE, None) == -1
 
 

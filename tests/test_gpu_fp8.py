@@ -136,10 +136,12 @@ def test_config4_outlier_accuracy_triad():
     assert api.device_status()[0] == 0
 
 
+@pytest.mark.parametrize("d", [64, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_head_dim_256_matches_oracle_on_dequantised_codes(causal):
-    """head_dim 256 (the pages' FP8 figure is for d = 256)."""
-    B, N, H, d = 1, 700, 2, 256
+def test_fp8_head_dim_256_matches_oracle_on_dequantised_codes(causal, d):
+    """head_dim 256 (the pages' FP8 figure is for d = 256) and 64 (64-byte
+    rows: the tiles use the 64-byte swizzle)."""
+    B, N, H = 1, 700, 2
     q, k, v = synth.qkv_bf16(B, N, H, d, seed=15, outliers=True)
     o, lse, (q8, k8, v8, qs, ks, vs) = _fp8_run(q, k, v, api.MODE_BLOCK_HADAMARD, causal=causal)
     rows = np.arange(N, dtype=np.int32)
@@ -151,11 +153,12 @@ def test_fp8_head_dim_256_matches_oracle_on_dequantised_codes(causal):
     assert api.device_status()[0] == 0
 
 
-def test_fp8_head_dim_256_outlier_accuracy():
-    """B=1, H=8, N=4096, d=256 non-causal on outlier inputs: error against
-    fp64 on the unquantised inputs within the FP8 bar, and below the
-    per-tensor baseline."""
-    B, N, H, d = 1, 4096, 8, 256
+@pytest.mark.parametrize("d", [64, 256])
+def test_fp8_head_dim_256_outlier_accuracy(d):
+    """B=1, N=4096, hidden 2048 (H = 2048 / d), non-causal on outlier inputs:
+    error against fp64 on the unquantised inputs within the FP8 bar, and
+    below the per-tensor baseline."""
+    B, N, H = 1, 4096, 2048 // d
     q, k, v = synth.qkv_bf16(B, N, H, d, seed=2, outliers=True)
     rows = synth.sample_rows(N, 48, seed=6)
     o_ref, _ = oracle.attention(q, k, v, rows=rows)
@@ -163,5 +166,5 @@ def test_fp8_head_dim_256_outlier_accuracy():
     for name, mode in (("per_tensor", api.MODE_PER_TENSOR), ("block_hadamard", api.MODE_BLOCK_HADAMARD)):
         o, lse, _ = _fp8_run(q, k, v, mode)
         rms[name] = float(np.sqrt(np.mean((gpu_rows(o, rows) - o_ref) ** 2)))
-    print("d=256 RMS vs fp64:", rms)
+    print(f"d={d} RMS vs fp64:", rms)
     assert rms["block_hadamard"] <= FP8_RMS and rms["block_hadamard"] < rms["per_tensor"], rms
