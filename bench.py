@@ -299,6 +299,26 @@ def time_loop(fn, steps, stream):
     return e0.elapsed_time(e1)
 
 
+def time_loop_two_streams(fn, steps, streams):
+    """time_loop for work spread over two streams: the start event is on the
+    first, the second waits for it; the end event is recorded on the first
+    after it has waited for everything queued on the second."""
+    import torch
+    a, b = streams
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(a)
+    b.wait_event(e0)
+    for _ in range(steps):
+        fn()
+    eb = torch.cuda.Event()
+    eb.record(b)
+    a.wait_event(eb)
+    e1.record(a)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def _oracle_inputs(w, arrs=None):
     from exact_attention_71_gb300 import synth
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
@@ -652,8 +672,31 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
     hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
     fp8 = w["dtype"] == "fp8"
     launches = 4 if fp8 else 1
+    host_path = not fp8 and hmask is None
+    if host_path:
+        # The library's host-buffer entry: chunks of sequences staged through
+        # two device slots, copies overlapping the forward (and the previous
+        # step's copies).
+        ws = torch.empty(api.fwd_host_workspace_bytes(B, H, H, N, d), dtype=torch.uint8, device=device)
+        seqs_per_chunk = -(-B // min(B, 4))
+        launches = -(-B // seqs_per_chunk)
+
+    # Host path: consecutive steps alternate between two streams (two requests
+    # in flight), so one step's input copies can start while the previous
+    # step's outputs are still coming back; each step's own copies and
+    # forward stay ordered on its stream.
+    streams = [stream, torch.cuda.Stream(device=device)]
+    host_out = [(ho, hl), (torch.empty_like(ho).pin_memory(), torch.empty_like(hl).pin_memory())]
+    turn = [0]
 
     def step():
+        if host_path:
+            s_ = streams[turn[0] & 1]
+            o_, l_ = host_out[turn[0] & 1]
+            turn[0] += 1
+            api.attn_fwd_host(hq, hk, hv, causal=w["causal"], window=w["window"], out=o_, lse=l_, workspace=ws,
+                              stream=s_)
+            return
         with torch.cuda.stream(stream):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
@@ -675,11 +718,17 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
     for _ in range(3):
         step()
     torch.cuda.synchronize(device)
-    ms = time_loop(step, steps, stream) / steps
+    if host_path:
+        ms = time_loop_two_streams(step, steps, streams) / steps
+    else:
+        ms = time_loop(step, steps, stream) / steps
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + (hmask.numel() if hmask is not None else 0)
     d2h = ho.numel() * 2 + hl.numel() * 4
-    return {"value": round(flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "kernel_launches_per_step": launches}
+    out = {"value": round(flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "kernel_launches_per_step": launches}
+    if host_path:
+        out["api"] = "attn_fwd_host (pinned host buffers; per-sequence chunks, copies overlapped with the forward)"
+    return out
 
 
 def bwd_secondary(api, device, stream, steps):

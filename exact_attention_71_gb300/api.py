@@ -66,6 +66,10 @@ def library() -> ctypes.CDLL:
         L.attn_bwd_noalloc.restype = i
         L.attn_bwd_noalloc_max_scratch.argtypes = []
         L.attn_bwd_noalloc_max_scratch.restype = sz
+        L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i]
+        L.attn_fwd_host_workspace_size.restype = sz
+        L.attn_fwd_host.argtypes = [P, P, P, P, P, i, i, i, i, i, i, f, i, P, sz, P]
+        L.attn_fwd_host.restype = i
         L.attn_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         L.attn_device_status.restype = i
         L.attn_set_wait_limit.argtypes = [u64]
@@ -142,6 +146,48 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, window: 
                                     int(bool(causal)), float(scale or 0.0), int(window),
                                     ctypes.c_void_p(_stream(stream)))
         _check("attn_fwd_gqa", rc)
+    return out, lse
+
+
+def fwd_host_workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int) -> int:
+    return int(library().attn_fwd_host_workspace_size(B, H, H_kv, N, d))
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0,
+                  out=None, lse=None, workspace=None, device=None, stream=None):
+    """attn_fwd on HOST tensors: q (B, N, H, d), k, v (B, N, H_kv, d) bf16 CPU
+    tensors (page-locked, e.g. ``.pin_memory()``, for overlapped copies).
+    The library stages chunks of sequences through ``workspace`` (a uint8
+    CUDA tensor of at least fwd_host_workspace_bytes(...) bytes, allocated
+    here when omitted) on ``device``.  Returns host (O, LSE); the call is
+    asynchronous on ``stream``: synchronize it before reading them.
+    """
+    for t in (q, k, v):
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v must be contiguous 4-d bf16 CPU tensors")
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != N or k.shape[3] != d or H % Hkv != 0:
+        raise ValueError("k, v must be (B, N, H_kv, d) with H_kv dividing the query heads")
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    if out.is_cuda or out.shape != (B, N, H, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 (B, N, H, d) CPU tensor")
+    if lse.is_cuda or lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 (B, H, N) CPU tensor")
+    device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    need = fwd_host_workspace_bytes(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    with torch.cuda.device(workspace.device):
+        rc = library().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                                     int(bool(causal)), float(scale or 0.0), int(window), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     ctypes.c_void_p(_stream(stream)))
+    _check("attn_fwd_host", rc)
     return out, lse
 
 
@@ -317,16 +363,6 @@ def device_status(stream=None):
     site = ctypes.c_int(0)
     rc = library().attn_device_status(ctypes.c_void_p(_stream(stream)), ctypes.byref(site))
     return rc, site.value
-
-
-def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, window: int = 0,
-                  device="cuda", stream=None):
-    """End-to-end call on HOST tensors: copies q, k, v to the device, runs
-    attn_fwd, and copies O and LSE back (pinned host buffers are used as-is)."""
-    dev = torch.device(device)
-    qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
-    o, lse = attn_fwd(qd, kd, vd, causal=causal, scale=scale, window=window, stream=stream)
-    return o.to("cpu"), lse.to("cpu")
 
 
 def default_scale(d: int) -> float:

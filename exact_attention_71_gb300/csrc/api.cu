@@ -486,3 +486,162 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// attn_fwd_host: the forward on host buffers (see include/attn.h).  Chunks of
+// whole sequences go through two device staging slots; per chunk c (slot
+// c % 2, counted per device across calls):
+//   h2d stream : wait freed[slot] (the D2H of the chunk that used the slot
+//                before), copy Q, K, V in, record loaded[slot]
+//   comp stream: wait loaded[slot], forward, record computed[slot]
+//   d2h stream : wait computed[slot], copy O, LSE out, record freed[slot]
+// so the copies in one direction overlap the forward and the copies in the
+// other direction of the neighbouring chunks.
+
+namespace {
+
+constexpr int kHostChunks = 4;   // chunks per call (at most B)
+
+struct HostPipe {
+    cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+    cudaEvent_t entry = nullptr, done = nullptr;
+    cudaEvent_t loaded[2] = {}, computed[2] = {}, freed[2] = {};
+    unsigned long long chunks = 0;
+    const void* last_ws = nullptr;   // staging layout of the previous call
+    size_t last_slot = 0;
+    bool ready = false;
+};
+
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mutex;   // guards g_pipe and the order of the enqueued work
+
+// Called with g_pipe_mutex held.
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    HostPipe& P = g_pipe[dev];
+    if (!P.ready) {
+        cudaStream_t* streams[3] = {&P.h2d, &P.comp, &P.d2h};
+        for (cudaStream_t* s : streams) {
+            if (*s) continue;
+            e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreateWithFlags");
+        }
+        cudaEvent_t* events[8] = {&P.entry, &P.done, &P.loaded[0], &P.loaded[1],
+                                  &P.computed[0], &P.computed[1], &P.freed[0], &P.freed[1]};
+        for (cudaEvent_t* ev : events) {
+            if (*ev) continue;
+            e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreateWithFlags");
+        }
+        P.ready = true;
+    }
+    *out = &P;
+    return ATTN_OK;
+}
+
+struct HostLayout {
+    long long cb;                       // sequences per chunk
+    size_t q_seq, kv_seq, l_seq;        // bytes of one sequence of Q (= O), K (= V), LSE
+    size_t off_k, off_v, off_o, off_l, slot;
+};
+
+bool host_layout(int B, int H, int H_kv, int N, int d, HostLayout* L) {
+    if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return false;
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const long long nch = B < kHostChunks ? B : kHostChunks;
+    L->cb = (B + nch - 1) / nch;
+    L->q_seq = static_cast<size_t>(N) * H * d * 2;
+    L->kv_seq = static_cast<size_t>(N) * H_kv * d * 2;
+    L->l_seq = static_cast<size_t>(H) * N * 4;
+    const size_t cb = static_cast<size_t>(L->cb);
+    L->off_k = up(cb * L->q_seq);
+    L->off_v = L->off_k + up(cb * L->kv_seq);
+    L->off_o = L->off_v + up(cb * L->kv_seq);
+    L->off_l = L->off_o + up(cb * L->q_seq);
+    L->slot = L->off_l + up(cb * L->l_seq);
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_fwd_host_workspace_size(int B, int H, int H_kv, int N, int d) {
+    HostLayout L;
+    if (!host_layout(B, H, H_kv, N, d, &L)) return 0;
+    return 2 * L.slot;
+}
+
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                  int d, int causal, float scale, int window, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+    g_err[0] = '\0';
+    int rc = check_common(q, k, v, o, lse, B, H, N, d, window);
+    if (rc != ATTN_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    HostLayout L;
+    host_layout(B, H, H_kv, N, d, &L);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < 2 * L.slot)
+        return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned and at least %zu bytes (got %zu)",
+                    2 * L.slot, workspace_bytes);
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe* P = nullptr;
+    if ((rc = host_pipe(&P)) != ATTN_OK) return rc;
+    const cudaStream_t user = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaEventRecord(P->entry, user);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(P->h2d, P->entry, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_host: ordering after the caller's stream");
+    // A call with another staging layout (workspace or slot size) than the
+    // previous one waits until both slots of the previous one are free: its
+    // slots need not coincide with the old ones.
+    if (P->last_ws != workspace || P->last_slot != L.slot) {
+        for (int s = 0; s < 2 && e == cudaSuccess; ++s) e = cudaStreamWaitEvent(P->h2d, P->freed[s], 0);
+        if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_host: ordering after the previous staging");
+        P->last_ws = workspace;
+        P->last_slot = L.slot;
+    }
+    const char* hq = static_cast<const char*>(q);
+    const char* hk = static_cast<const char*>(k);
+    const char* hv = static_cast<const char*>(v);
+    char* ho = static_cast<char*>(o);
+    char* hl = reinterpret_cast<char*>(lse);
+    for (long long b0 = 0; b0 < B && rc == ATTN_OK; b0 += L.cb) {
+        const long long nb = B - b0 < L.cb ? B - b0 : L.cb;
+        const int slot = static_cast<int>(P->chunks & 1);
+        ++P->chunks;
+        char* base = static_cast<char*>(workspace) + slot * L.slot;
+        char *dq = base, *dk = base + L.off_k, *dv = base + L.off_v, *dout = base + L.off_o, *dl = base + L.off_l;
+        const size_t qb = nb * L.q_seq, kvb = nb * L.kv_seq, lb = nb * L.l_seq;
+        e = cudaStreamWaitEvent(P->h2d, P->freed[slot], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dq, hq + b0 * L.q_seq, qb, cudaMemcpyHostToDevice, P->h2d);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dk, hk + b0 * L.kv_seq, kvb, cudaMemcpyHostToDevice, P->h2d);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(dv, hv + b0 * L.kv_seq, kvb, cudaMemcpyHostToDevice, P->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(P->loaded[slot], P->h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(P->comp, P->loaded[slot], 0);
+        if (e != cudaSuccess) {
+            rc = cuda_fail(e, "attn_fwd_host: host-to-device copy");
+            break;
+        }
+        rc = launch_forward(false, dq, dk, dv, dout, reinterpret_cast<float*>(dl), static_cast<int>(nb), H, H_kv, N,
+                            d, causal, scale, window, nullptr, nullptr, nullptr, P->comp);
+        if (rc != ATTN_OK) break;
+        e = cudaEventRecord(P->computed[slot], P->comp);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(P->d2h, P->computed[slot], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(ho + b0 * L.q_seq, dout, qb, cudaMemcpyDeviceToHost, P->d2h);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(hl + b0 * L.l_seq, dl, lb, cudaMemcpyDeviceToHost, P->d2h);
+        if (e == cudaSuccess) e = cudaEventRecord(P->freed[slot], P->d2h);
+        if (e != cudaSuccess) rc = cuda_fail(e, "attn_fwd_host: device-to-host copy");
+    }
+    // The caller's stream resumes after everything queued above.
+    e = cudaEventRecord(P->done, P->d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(user, P->done, 0);
+    if (e != cudaSuccess && rc == ATTN_OK) rc = cuda_fail(e, "attn_fwd_host: ordering the caller's stream");
+    return rc;
+}
+
+}  // extern "C"

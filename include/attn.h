@@ -174,6 +174,40 @@ int attn_fwd_sparse(const void* q, const void* k, const void* v, void* o, float*
                     int causal, float scale, int window, void* stream);
 
 /*
+ * attn_fwd_host_workspace_size / attn_fwd_host -- attn_fwd_gqa on HOST
+ * buffers.  The pages' forward reads Q, K, V from and writes O, LSE to device
+ * memory; this entry is the same computation for a caller whose tensors live
+ * in host memory (no counterpart in the pages).  The batch is cut into
+ * chunks of whole sequences; for each chunk the library copies Q, K, V to
+ * one of two device staging slots, runs the forward on it and copies O and
+ * LSE back, with the copies of one chunk overlapping the forward and the
+ * copies of its neighbours (three library-owned streams, created once per
+ * device; events order them).  Consecutive calls overlap the same way.
+ *   q, k, v, o, lse : HOST pointers with the layouts of attn_fwd_gqa
+ *                     (16-byte aligned; page-locked memory, e.g. from
+ *                     cudaHostAlloc, is what lets the copies overlap)
+ *   workspace       : device, at least attn_fwd_host_workspace_size(B, H,
+ *                     H_kv, N, d) bytes, 256-byte aligned, owned by the
+ *                     caller (the two staging slots)
+ *   B, H, H_kv, N, d, causal, scale, window : as attn_fwd_gqa
+ * The call is asynchronous on `stream`: its copies start after the work
+ * already queued on `stream`, and work queued on `stream` afterwards starts
+ * after O and LSE are in host memory, so the caller synchronizes `stream`
+ * before reading them and keeps the buffers alive until then.  Calls may
+ * share a workspace, on any streams: the library orders the reuse of its
+ * staging slots (two calls in flight on two streams overlap the copies of
+ * one with those of the other).  Errors: as attn_fwd_gqa;
+ * a NULL, unaligned or too small workspace is ATTN_ERR_INVALID_ARG;
+ * ATTN_ERR_CUDA if a copy or a launch fails part-way (the chunks queued
+ * before it still complete in order on `stream`).
+ * attn_fwd_host_workspace_size returns 0 for invalid sizes.
+ */
+size_t attn_fwd_host_workspace_size(int B, int H, int H_kv, int N, int d);
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int H_kv, int N, int d, int causal, float scale, int window, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_workspace_size / attn_bwd -- backward of attn_fwd / attn_fwd_gqa
  * (deep-reading report §3.4: FA3 keeps FA2's recompute strategy; five
  * matrix products against the forward's two).  For a loss L with upstream

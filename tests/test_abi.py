@@ -123,3 +123,28 @@ def test_sparse_arguments_checked(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 3, 100, 128, 0, 0.0, 0, None) == -1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 2, 100, 96, 0, 0.0, 0, None) == -2
     assert f(None, None, None, None, None, None, 1, 2, 2, 0, 128, 0, 0.0, 0, None) == 0
+
+
+def test_host_forward_workspace_and_arguments(lib):
+    """attn_fwd_host: two staging slots of whole-sequence chunks (at most four
+    chunks per call); its argument checks run before any CUDA call."""
+    size = lib.attn_fwd_host_workspace_size
+    # B=3 -> 3 chunks of 1 sequence: Q, K, V, O, LSE parts rounded to 256 bytes
+    q_seq, kv_seq, l_seq = 100 * 2 * 128 * 2, 100 * 1 * 128 * 2, 2 * 100 * 4
+    up = lambda x: (x + 255) // 256 * 256
+    slot = 2 * up(q_seq) + 2 * up(kv_seq) + up(l_seq)
+    assert size(3, 2, 1, 100, 128) == 2 * slot
+    # B=10 -> chunks of ceil(10 / 4) = 3 sequences
+    assert size(10, 2, 1, 100, 128) == 2 * (2 * up(3 * q_seq) + 2 * up(3 * kv_seq) + up(3 * l_seq))
+    assert size(-1, 2, 1, 100, 128) == 0 and size(1, 2, 0, 100, 128) == 0
+    f = lib.attn_fwd_host
+    ws = size(3, 2, 1, 100, 128)
+    args = lambda d=128, hkv=1, wsp=FAKE, wsb=ws: (FAKE, FAKE, FAKE, FAKE, FAKE, 3, 2, hkv, 100, d, 1, 0.0, 0, wsp,
+                                                   wsb, None)
+    assert f(*args(d=96)) == -2
+    assert f(*args(hkv=3)) == -1
+    assert f(*args(wsp=None)) == -1
+    assert f(*args(wsp=ctypes.c_void_p((1 << 20) + 16))) == -1
+    assert b"256-byte" in lib.attn_last_error_string()
+    assert f(*args(wsb=ws - 1)) == -1
+    assert f(None, None, None, None, None, 0, 2, 1, 100, 128, 0, 0.0, 0, None, 0, None) == 0

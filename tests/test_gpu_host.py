@@ -1,0 +1,91 @@
+"""attn_fwd_host (the forward on host buffers, chunked through two device
+staging slots) returns exactly what attn_fwd returns on the same data, for
+ragged chunkings, grouped heads, masks and back-to-back calls that overlap."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_71_gb300 import api, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def host_qkv(B, N, H, Hkv, d, seed, pin=True):
+    q = synth.tensor_bf16((B, N, H, d), seed=seed, stream=1)
+    k = synth.tensor_bf16((B, N, Hkv, d), seed=seed, stream=2)
+    v = synth.tensor_bf16((B, N, Hkv, d), seed=seed, stream=3)
+    t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    out = tuple(t(a) for a in (q, k, v))
+    return tuple(x.pin_memory() for x in out) if pin else out
+
+
+@pytest.mark.parametrize("B,N,H,Hkv,d,causal,window", [
+    (3, 1000, 4, 2, 128, True, 0),      # 3 chunks of 1 sequence, grouped heads, ragged N
+    (5, 777, 2, 2, 64, False, 0),       # chunks of 2, 2, 1
+    (1, 300, 2, 1, 256, True, 100),     # one chunk, multi-query, sliding window
+    (9, 512, 8, 8, 128, True, 0),       # chunks of 3
+])
+def test_host_forward_matches_device_forward(B, N, H, Hkv, d, causal, window):
+    q, k, v = host_qkv(B, N, H, Hkv, d, seed=B * 100 + d)
+    o, lse = api.attn_fwd_host(q, k, v, causal=causal, window=window)
+    torch.cuda.synchronize()
+    dev = torch.device("cuda:0")
+    o_ref, lse_ref = api.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal, window=window)
+    torch.cuda.synchronize()
+    assert api.device_status() == (0, 0)
+    assert torch.equal(o.view(torch.int16), o_ref.cpu().view(torch.int16))
+    assert torch.equal(lse, lse_ref.cpu())
+
+
+def test_host_forward_against_oracle():
+    B, N, H, d = 2, 200, 2, 64
+    q, k, v = host_qkv(B, N, H, H, d, seed=7)
+    o, lse = api.attn_fwd_host(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    as_np = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    o_ref, lse_ref = oracle.attention(as_np(q), as_np(k), as_np(v), causal=True)
+    err = np.abs(o.float().permute(0, 2, 1, 3).double().numpy() - o_ref)
+    assert err.max() <= 1e-2 and np.sqrt(np.mean(err ** 2)) <= 2e-3
+    assert np.abs(lse.double().numpy() - lse_ref).max() <= 1e-3
+
+
+def test_back_to_back_calls_and_pageable_memory():
+    """Calls queued without a synchronisation in between share the staging
+    slots (their copies overlap); each still gets its own result.  Pageable
+    host memory works too (the copies then do not overlap)."""
+    dev = torch.device("cuda:0")
+    B, N, H, d = 4, 640, 4, 128
+    ws = torch.empty(api.fwd_host_workspace_bytes(B, H, H, N, d), dtype=torch.uint8, device=dev)
+    runs = []
+    for i in range(5):
+        q, k, v = host_qkv(B, N, H, H, d, seed=50 + i, pin=(i != 3))
+        runs.append(((q, k, v), api.attn_fwd_host(q, k, v, causal=bool(i & 1), workspace=ws)))
+    torch.cuda.synchronize()
+    for i, ((q, k, v), (o, lse)) in enumerate(runs):
+        o_ref, lse_ref = api.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=bool(i & 1))
+        assert torch.equal(o.view(torch.int16), o_ref.cpu().view(torch.int16)), i
+        assert torch.equal(lse, lse_ref.cpu()), i
+    assert api.device_status() == (0, 0)
+
+
+def test_two_streams_and_changing_shapes_share_a_workspace():
+    """Calls in flight on two streams share one workspace, and calls of
+    different shapes (different staging layouts) follow each other without a
+    synchronisation; every result matches the device forward."""
+    dev = torch.device("cuda:0")
+    shapes = [(2, 1024, 8, 128), (3, 500, 4, 64), (2, 1024, 8, 128), (1, 2048, 2, 256), (4, 256, 8, 128)]
+    ws = torch.empty(max(api.fwd_host_workspace_bytes(B, H, H, N, d) for B, N, H, d in shapes),
+                     dtype=torch.uint8, device=dev)
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    runs = []
+    for i, (B, N, H, d) in enumerate(shapes * 2):
+        q, k, v = host_qkv(B, N, H, H, d, seed=200 + i)
+        runs.append(((q, k, v), i, api.attn_fwd_host(q, k, v, causal=bool(i % 3), workspace=ws,
+                                                      stream=streams[i & 1])))
+    torch.cuda.synchronize()
+    for (q, k, v), i, (o, lse) in runs:
+        o_ref, lse_ref = api.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=bool(i % 3))
+        assert torch.equal(o.view(torch.int16), o_ref.cpu().view(torch.int16)), i
+        assert torch.equal(lse, lse_ref.cpu()), i
+    assert api.device_status() == (0, 0)
