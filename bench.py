@@ -672,14 +672,15 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
     hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
     fp8 = w["dtype"] == "fp8"
     launches = 4 if fp8 else 1
-    host_path = not fp8 and hmask is None
+    host_path = hmask is None
     if host_path:
-        # The library's host-buffer entry: chunks of sequences staged through
-        # two device slots, copies overlapping the forward (and the previous
-        # step's copies).
-        ws = torch.empty(api.fwd_host_workspace_bytes(B, H, H, N, d), dtype=torch.uint8, device=device)
+        # The library's host-buffer entries: chunks of sequences staged
+        # through two device slots, copies overlapping the compute (and the
+        # previous step's copies).  FP8: prep of Q, K, V + forward per chunk.
+        wsb = (api.fwd_fp8_host_workspace_bytes if fp8 else api.fwd_host_workspace_bytes)(B, H, H, N, d)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=device)
         seqs_per_chunk = -(-B // min(B, 4))
-        launches = -(-B // seqs_per_chunk)
+        launches = -(-B // seqs_per_chunk) * (4 if fp8 else 1)
 
     # Host path: consecutive steps alternate between two streams (two requests
     # in flight), so one step's input copies can start while the previous
@@ -694,8 +695,12 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
             s_ = streams[turn[0] & 1]
             o_, l_ = host_out[turn[0] & 1]
             turn[0] += 1
-            api.attn_fwd_host(hq, hk, hv, causal=w["causal"], window=w["window"], out=o_, lse=l_, workspace=ws,
-                              stream=s_)
+            if fp8:
+                api.attn_fwd_fp8_host(hq, hk, hv, api.MODE_BLOCK_HADAMARD, 1234, causal=w["causal"],
+                                      window=w["window"], out=o_, lse=l_, workspace=ws, stream=s_)
+            else:
+                api.attn_fwd_host(hq, hk, hv, causal=w["causal"], window=w["window"], out=o_, lse=l_, workspace=ws,
+                                  stream=s_)
             return
         with torch.cuda.stream(stream):
             dq.copy_(hq, non_blocking=True)
@@ -727,7 +732,8 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
     out = {"value": round(flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "kernel_launches_per_step": launches}
     if host_path:
-        out["api"] = "attn_fwd_host (pinned host buffers; per-sequence chunks, copies overlapped with the forward)"
+        out["api"] = (("attn_fwd_fp8_host" if fp8 else "attn_fwd_host") +
+                      " (pinned host buffers; per-sequence chunks, copies overlapped with the compute; two streams)")
     return out
 
 

@@ -70,6 +70,10 @@ def library() -> ctypes.CDLL:
         L.attn_fwd_host_workspace_size.restype = sz
         L.attn_fwd_host.argtypes = [P, P, P, P, P, i, i, i, i, i, i, f, i, P, sz, P]
         L.attn_fwd_host.restype = i
+        L.attn_fwd_fp8_host_workspace_size.argtypes = [i, i, i, i, i]
+        L.attn_fwd_fp8_host_workspace_size.restype = sz
+        L.attn_fwd_fp8_host.argtypes = [P, P, P, P, P, i, i, i, i, i, i, f, i, i, u64, P, sz, P]
+        L.attn_fwd_fp8_host.restype = i
         L.attn_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         L.attn_device_status.restype = i
         L.attn_set_wait_limit.argtypes = [u64]
@@ -162,6 +166,25 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, win
     here when omitted) on ``device``.  Returns host (O, LSE); the call is
     asynchronous on ``stream``: synchronize it before reading them.
     """
+    B, N, H, Hkv, d, out, lse = _host_args(q, k, v, out, lse)
+    device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    need = fwd_host_workspace_bytes(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    with torch.cuda.device(workspace.device):
+        rc = library().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                                     int(bool(causal)), float(scale or 0.0), int(window), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     ctypes.c_void_p(_stream(stream)))
+    _check("attn_fwd_host", rc)
+    return out, lse
+
+
+def fwd_fp8_host_workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int) -> int:
+    return int(library().attn_fwd_fp8_host_workspace_size(B, H, H_kv, N, d))
+
+
+def _host_args(q, k, v, out, lse):
     for t in (q, k, v):
         if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
             raise ValueError("q, k, v must be contiguous 4-d bf16 CPU tensors")
@@ -178,16 +201,27 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, win
         raise ValueError("out must be a contiguous bf16 (B, N, H, d) CPU tensor")
     if lse.is_cuda or lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 (B, H, N) CPU tensor")
+    return B, N, H, Hkv, d, out, lse
+
+
+def attn_fwd_fp8_host(q, k, v, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0, causal: bool = False,
+                      scale: float | None = None, window: int = 0, out=None, lse=None, workspace=None, device=None,
+                      stream=None):
+    """The FP8 path on HOST bf16 tensors (prep + e4m3 forward per chunk of
+    sequences, staged and overlapped like attn_fwd_host).  mode: MODE_BLOCK or
+    MODE_BLOCK_HADAMARD.  Returns host (O, LSE); asynchronous on ``stream``."""
+    B, N, H, Hkv, d, out, lse = _host_args(q, k, v, out, lse)
     device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    need = fwd_host_workspace_bytes(B, H, Hkv, N, d)
     if workspace is None:
+        need = fwd_fp8_host_workspace_bytes(B, H, Hkv, N, d)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
     with torch.cuda.device(workspace.device):
-        rc = library().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
-                                     int(bool(causal)), float(scale or 0.0), int(window), _ptr(workspace),
-                                     workspace.numel() * workspace.element_size(),
-                                     ctypes.c_void_p(_stream(stream)))
-    _check("attn_fwd_host", rc)
+        rc = library().attn_fwd_fp8_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
+                                         int(bool(causal)), float(scale or 0.0), int(window), int(mode),
+                                         int(sign_seed) & 0xFFFFFFFFFFFFFFFF, _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         ctypes.c_void_p(_stream(stream)))
+    _check("attn_fwd_fp8_host", rc)
     return out, lse
 
 

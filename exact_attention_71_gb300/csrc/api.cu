@@ -542,27 +542,102 @@ int host_pipe(HostPipe** out) {
     return ATTN_OK;
 }
 
-struct HostLayout {
-    long long cb;                       // sequences per chunk
-    size_t q_seq, kv_seq, l_seq;        // bytes of one sequence of Q (= O), K (= V), LSE
-    size_t off_k, off_v, off_o, off_l, slot;
+// Staging layout of one slot: the chunk's inputs (Q, K, V), outputs (O,
+// LSE) and the scratch its compute step uses, each part 256-byte aligned.
+struct Staging {
+    long long cb = 0;                  // sequences per chunk
+    size_t in_seq[3] = {}, out_seq[2] = {};
+    size_t in_off[3] = {}, out_off[2] = {}, scratch_off = 0, slot = 0;
 };
 
-bool host_layout(int B, int H, int H_kv, int N, int d, HostLayout* L) {
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Q, K, V in and O, LSE out for (B, N, H / H_kv, d) bf16 tensors, plus
+// `scratch_per_seq` bytes of scratch parts (each rounded per chunk).
+bool staging(int B, int H, int H_kv, int N, int d, const size_t* scratch_per_seq, int n_scratch, Staging* L) {
     if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return false;
-    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const long long nch = B < kHostChunks ? B : kHostChunks;
     L->cb = (B + nch - 1) / nch;
-    L->q_seq = static_cast<size_t>(N) * H * d * 2;
-    L->kv_seq = static_cast<size_t>(N) * H_kv * d * 2;
-    L->l_seq = static_cast<size_t>(H) * N * 4;
     const size_t cb = static_cast<size_t>(L->cb);
-    L->off_k = up(cb * L->q_seq);
-    L->off_v = L->off_k + up(cb * L->kv_seq);
-    L->off_o = L->off_v + up(cb * L->kv_seq);
-    L->off_l = L->off_o + up(cb * L->q_seq);
-    L->slot = L->off_l + up(cb * L->l_seq);
+    const size_t q_seq = static_cast<size_t>(N) * H * d * 2, kv_seq = static_cast<size_t>(N) * H_kv * d * 2;
+    L->in_seq[0] = q_seq;
+    L->in_seq[1] = L->in_seq[2] = kv_seq;
+    L->out_seq[0] = q_seq;
+    L->out_seq[1] = static_cast<size_t>(H) * N * 4;
+    size_t off = 0;
+    for (int x = 0; x < 3; ++x) { L->in_off[x] = off; off += up256(cb * L->in_seq[x]); }
+    for (int x = 0; x < 2; ++x) { L->out_off[x] = off; off += up256(cb * L->out_seq[x]); }
+    L->scratch_off = off;
+    for (int x = 0; x < n_scratch; ++x) off += up256(cb * scratch_per_seq[x]);
+    L->slot = off;
     return true;
+}
+
+// Runs the chunks of one call through the staging slots (see above).
+// compute(nb, slot_base, stream) queues the chunk's work on `stream`.
+template <class Compute>
+int host_pipeline(const void* const in[3], void* const out[2], int B, const Staging& L, void* workspace,
+                  size_t workspace_bytes, void* stream, const char* who, Compute&& compute) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < 2 * L.slot)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned and at least %zu bytes (got %zu)",
+                    who, 2 * L.slot, workspace_bytes);
+    std::lock_guard<std::mutex> lock(g_pipe_mutex);
+    HostPipe* P = nullptr;
+    int rc = host_pipe(&P);
+    if (rc != ATTN_OK) return rc;
+    const cudaStream_t user = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaEventRecord(P->entry, user);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(P->h2d, P->entry, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "host pipeline: ordering after the caller's stream");
+    // A call with another staging layout (workspace or slot size) than the
+    // previous one waits until both slots of the previous one are free: its
+    // slots need not coincide with the old ones.
+    if (P->last_ws != workspace || P->last_slot != L.slot) {
+        for (int s = 0; s < 2 && e == cudaSuccess; ++s) e = cudaStreamWaitEvent(P->h2d, P->freed[s], 0);
+        if (e != cudaSuccess) return cuda_fail(e, "host pipeline: ordering after the previous staging");
+        P->last_ws = workspace;
+        P->last_slot = L.slot;
+    }
+    for (long long b0 = 0; b0 < B && rc == ATTN_OK; b0 += L.cb) {
+        const long long nb = B - b0 < L.cb ? B - b0 : L.cb;
+        const int slot = static_cast<int>(P->chunks & 1);
+        ++P->chunks;
+        char* base = static_cast<char*>(workspace) + slot * L.slot;
+        e = cudaStreamWaitEvent(P->h2d, P->freed[slot], 0);
+        for (int x = 0; x < 3 && e == cudaSuccess; ++x)
+            e = cudaMemcpyAsync(base + L.in_off[x], static_cast<const char*>(in[x]) + b0 * L.in_seq[x],
+                                nb * L.in_seq[x], cudaMemcpyHostToDevice, P->h2d);
+        if (e == cudaSuccess) e = cudaEventRecord(P->loaded[slot], P->h2d);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(P->comp, P->loaded[slot], 0);
+        if (e != cudaSuccess) {
+            rc = cuda_fail(e, "host pipeline: host-to-device copy");
+            break;
+        }
+        rc = compute(static_cast<int>(nb), base, P->comp);
+        if (rc != ATTN_OK) break;
+        e = cudaEventRecord(P->computed[slot], P->comp);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(P->d2h, P->computed[slot], 0);
+        for (int x = 0; x < 2 && e == cudaSuccess; ++x)
+            e = cudaMemcpyAsync(static_cast<char*>(out[x]) + b0 * L.out_seq[x], base + L.out_off[x],
+                                nb * L.out_seq[x], cudaMemcpyDeviceToHost, P->d2h);
+        if (e == cudaSuccess) e = cudaEventRecord(P->freed[slot], P->d2h);
+        if (e != cudaSuccess) rc = cuda_fail(e, "host pipeline: device-to-host copy");
+    }
+    // The caller's stream resumes after everything queued above.
+    e = cudaEventRecord(P->done, P->d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(user, P->done, 0);
+    if (e != cudaSuccess && rc == ATTN_OK) rc = cuda_fail(e, "host pipeline: ordering the caller's stream");
+    return rc;
+}
+
+// Scratch of the FP8 host forward per sequence: Q8, K8, V8 codes and the
+// three block-scale arrays.
+void fp8_scratch(int H, int H_kv, int N, int d, size_t s[6]) {
+    const size_t nblk = (static_cast<size_t>(N) + 127) / 128;
+    s[0] = static_cast<size_t>(N) * H * d;
+    s[1] = s[2] = static_cast<size_t>(N) * H_kv * d;
+    s[3] = static_cast<size_t>(H) * nblk * 4;
+    s[4] = s[5] = static_cast<size_t>(H_kv) * nblk * 4;
 }
 
 }  // namespace
@@ -570,8 +645,8 @@ bool host_layout(int B, int H, int H_kv, int N, int d, HostLayout* L) {
 extern "C" {
 
 size_t attn_fwd_host_workspace_size(int B, int H, int H_kv, int N, int d) {
-    HostLayout L;
-    if (!host_layout(B, H, H_kv, N, d, &L)) return 0;
+    Staging L;
+    if (!staging(B, H, H_kv, N, d, nullptr, 0, &L)) return 0;
     return 2 * L.slot;
 }
 
@@ -584,64 +659,67 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
     if (H_kv <= 0 || H % H_kv != 0)
         return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
     if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
-    HostLayout L;
-    host_layout(B, H, H_kv, N, d, &L);
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < 2 * L.slot)
-        return fail(ATTN_ERR_INVALID_ARG, "workspace must be 256-byte aligned and at least %zu bytes (got %zu)",
-                    2 * L.slot, workspace_bytes);
-    std::lock_guard<std::mutex> lock(g_pipe_mutex);
-    HostPipe* P = nullptr;
-    if ((rc = host_pipe(&P)) != ATTN_OK) return rc;
-    const cudaStream_t user = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaEventRecord(P->entry, user);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(P->h2d, P->entry, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_host: ordering after the caller's stream");
-    // A call with another staging layout (workspace or slot size) than the
-    // previous one waits until both slots of the previous one are free: its
-    // slots need not coincide with the old ones.
-    if (P->last_ws != workspace || P->last_slot != L.slot) {
-        for (int s = 0; s < 2 && e == cudaSuccess; ++s) e = cudaStreamWaitEvent(P->h2d, P->freed[s], 0);
-        if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_host: ordering after the previous staging");
-        P->last_ws = workspace;
-        P->last_slot = L.slot;
-    }
-    const char* hq = static_cast<const char*>(q);
-    const char* hk = static_cast<const char*>(k);
-    const char* hv = static_cast<const char*>(v);
-    char* ho = static_cast<char*>(o);
-    char* hl = reinterpret_cast<char*>(lse);
-    for (long long b0 = 0; b0 < B && rc == ATTN_OK; b0 += L.cb) {
-        const long long nb = B - b0 < L.cb ? B - b0 : L.cb;
-        const int slot = static_cast<int>(P->chunks & 1);
-        ++P->chunks;
-        char* base = static_cast<char*>(workspace) + slot * L.slot;
-        char *dq = base, *dk = base + L.off_k, *dv = base + L.off_v, *dout = base + L.off_o, *dl = base + L.off_l;
-        const size_t qb = nb * L.q_seq, kvb = nb * L.kv_seq, lb = nb * L.l_seq;
-        e = cudaStreamWaitEvent(P->h2d, P->freed[slot], 0);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(dq, hq + b0 * L.q_seq, qb, cudaMemcpyHostToDevice, P->h2d);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(dk, hk + b0 * L.kv_seq, kvb, cudaMemcpyHostToDevice, P->h2d);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(dv, hv + b0 * L.kv_seq, kvb, cudaMemcpyHostToDevice, P->h2d);
-        if (e == cudaSuccess) e = cudaEventRecord(P->loaded[slot], P->h2d);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(P->comp, P->loaded[slot], 0);
-        if (e != cudaSuccess) {
-            rc = cuda_fail(e, "attn_fwd_host: host-to-device copy");
-            break;
-        }
-        rc = launch_forward(false, dq, dk, dv, dout, reinterpret_cast<float*>(dl), static_cast<int>(nb), H, H_kv, N,
-                            d, causal, scale, window, nullptr, nullptr, nullptr, P->comp);
-        if (rc != ATTN_OK) break;
-        e = cudaEventRecord(P->computed[slot], P->comp);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(P->d2h, P->computed[slot], 0);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(ho + b0 * L.q_seq, dout, qb, cudaMemcpyDeviceToHost, P->d2h);
-        if (e == cudaSuccess) e = cudaMemcpyAsync(hl + b0 * L.l_seq, dl, lb, cudaMemcpyDeviceToHost, P->d2h);
-        if (e == cudaSuccess) e = cudaEventRecord(P->freed[slot], P->d2h);
-        if (e != cudaSuccess) rc = cuda_fail(e, "attn_fwd_host: device-to-host copy");
-    }
-    // The caller's stream resumes after everything queued above.
-    e = cudaEventRecord(P->done, P->d2h);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(user, P->done, 0);
-    if (e != cudaSuccess && rc == ATTN_OK) rc = cuda_fail(e, "attn_fwd_host: ordering the caller's stream");
-    return rc;
+    Staging L;
+    staging(B, H, H_kv, N, d, nullptr, 0, &L);
+    const void* in[3] = {q, k, v};
+    void* out[2] = {o, lse};
+    return host_pipeline(in, out, B, L, workspace, workspace_bytes, stream, "attn_fwd_host",
+                         [&](int nb, char* base, cudaStream_t s) {
+                             return launch_forward(false, base + L.in_off[0], base + L.in_off[1], base + L.in_off[2],
+                                                   base + L.out_off[0], reinterpret_cast<float*>(base + L.out_off[1]),
+                                                   nb, H, H_kv, N, d, causal, scale, window, nullptr, nullptr,
+                                                   nullptr, s);
+                         });
+}
+
+size_t attn_fwd_fp8_host_workspace_size(int B, int H, int H_kv, int N, int d) {
+    Staging L;
+    size_t sc[6];
+    if (H <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return 0;
+    fp8_scratch(H, H_kv, N, d, sc);
+    if (!staging(B, H, H_kv, N, d, sc, 6, &L)) return 0;
+    return 2 * L.slot;
+}
+
+int attn_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+                      int N, int d, int causal, float scale, int window, int mode, unsigned long long sign_seed,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = '\0';
+    int rc = check_common(q, k, v, o, lse, B, H, N, d, window);
+    if (rc != ATTN_OK) return rc;
+    if (H_kv <= 0 || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
+    if (mode != 0 && mode != 1)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8_host: mode %d (0 or 1; the per-tensor mode spans chunks)",
+                    mode);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    Staging L;
+    size_t sc[6];
+    fp8_scratch(H, H_kv, N, d, sc);
+    staging(B, H, H_kv, N, d, sc, 6, &L);
+    size_t soff[6];
+    for (int x = 0; x < 6; ++x)
+        soff[x] = x == 0 ? L.scratch_off : soff[x - 1] + up256(static_cast<size_t>(L.cb) * sc[x - 1]);
+    const void* in[3] = {q, k, v};
+    void* out[2] = {o, lse};
+    return host_pipeline(in, out, B, L, workspace, workspace_bytes, stream, "attn_fwd_fp8_host",
+                         [&](int nb, char* base, cudaStream_t s) {
+                             float* qs = reinterpret_cast<float*>(base + soff[3]);
+                             float* ks = reinterpret_cast<float*>(base + soff[4]);
+                             float* vs = reinterpret_cast<float*>(base + soff[5]);
+                             int r = attn_fp8_prep(base + L.in_off[0], base + soff[0], qs, nb, H, N, d, 128, mode,
+                                                   sign_seed, 0, s);
+                             if (r == ATTN_OK)
+                                 r = attn_fp8_prep(base + L.in_off[1], base + soff[1], ks, nb, H_kv, N, d, 128, mode,
+                                                   sign_seed, 0, s);
+                             if (r == ATTN_OK)
+                                 r = attn_fp8_prep(base + L.in_off[2], base + soff[2], vs, nb, H_kv, N, d, 128, mode,
+                                                   sign_seed, 1, s);
+                             if (r != ATTN_OK) return r;
+                             return launch_forward(true, base + soff[0], base + soff[1], base + soff[2],
+                                                   base + L.out_off[0], reinterpret_cast<float*>(base + L.out_off[1]),
+                                                   nb, H, H_kv, N, d, causal, scale, window, qs, ks, vs, s);
+                         });
 }
 
 }  // extern "C"

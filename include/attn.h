@@ -208,6 +208,29 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
                   size_t workspace_bytes, void* stream);
 
 /*
+ * attn_fwd_fp8_host_workspace_size / attn_fwd_fp8_host -- the FP8 path on
+ * HOST buffers: per chunk of sequences, the bf16 Q, K, V copied in are
+ * prepared (attn_fp8_prep with `mode` and `sign_seed`: Q and K rotated in mode
+ * 1, V never) and fed to attn_fwd_fp8_gqa, and O, LSE are copied back, staged
+ * and overlapped exactly as attn_fwd_host (no counterpart in the pages).
+ *   q, k, v         : HOST bf16 (B, N, H / H_kv, d), as attn_fwd_host
+ *   o, lse          : HOST outputs, as attn_fwd_host
+ *   mode            : 0 (per-block scales) or 1 (per-block scales after the
+ *                     rotation); the per-tensor mode 2 is refused
+ *                     (ATTN_ERR_INVALID_ARG) since its one scale would span
+ *                     chunks
+ *   workspace       : device, at least attn_fwd_fp8_host_workspace_size(B, H,
+ *                     H_kv, N, d) bytes, 256-byte aligned (the two slots also
+ *                     hold the e4m3 codes and block scales of their chunk)
+ * d must be 64, 128 or 256.  Ordering, sharing and errors as attn_fwd_host.
+ */
+size_t attn_fwd_fp8_host_workspace_size(int B, int H, int H_kv, int N, int d);
+int attn_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int H_kv, int N, int d, int causal, float scale, int window, int mode,
+                      unsigned long long sign_seed, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/*
  * attn_bwd_workspace_size / attn_bwd -- backward of attn_fwd / attn_fwd_gqa
  * (deep-reading report §3.4: FA3 keeps FA2's recompute strategy; five
  * matrix products against the forward's two).  For a loss L with upstream

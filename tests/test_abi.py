@@ -148,3 +148,26 @@ def test_host_forward_workspace_and_arguments(lib):
     assert b"256-byte" in lib.attn_last_error_string()
     assert f(*args(wsb=ws - 1)) == -1
     assert f(None, None, None, None, None, 0, 2, 1, 100, 128, 0, 0.0, 0, None, 0, None) == 0
+
+
+def test_fp8_host_forward_workspace_and_arguments(lib):
+    """attn_fwd_fp8_host: the slots of attn_fwd_host plus each chunk's e4m3
+    codes and block scales; the per-tensor mode is refused (its one scale
+    would span chunks)."""
+    size = lib.attn_fwd_fp8_host_workspace_size
+    up = lambda x: (x + 255) // 256 * 256
+    B, H, Hkv, N, d = 3, 2, 1, 100, 128
+    bf16_slot = lib.attn_fwd_host_workspace_size(B, H, Hkv, N, d) // 2
+    nblk = 1
+    codes = up(N * H * d) + 2 * up(N * Hkv * d)
+    scales = up(H * nblk * 4) + 2 * up(Hkv * nblk * 4)
+    assert size(B, H, Hkv, N, d) == 2 * (bf16_slot + codes + scales)
+    assert size(0, H, Hkv, N, d) == 0
+    f = lib.attn_fwd_fp8_host
+    ws = size(B, H, Hkv, N, d)
+    args = lambda mode=1, d=128, wsb=ws: (FAKE, FAKE, FAKE, FAKE, FAKE, B, H, Hkv, N, d, 0, 0.0, 0, mode, 7, FAKE,
+                                          wsb, None)
+    assert f(*args(mode=2)) == -1
+    assert b"mode" in lib.attn_last_error_string()
+    assert f(*args(d=96)) == -2
+    assert f(*args(wsb=ws - 1)) == -1

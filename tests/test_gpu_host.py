@@ -89,3 +89,52 @@ def test_two_streams_and_changing_shapes_share_a_workspace():
         assert torch.equal(o.view(torch.int16), o_ref.cpu().view(torch.int16)), i
         assert torch.equal(lse, lse_ref.cpu()), i
     assert api.device_status() == (0, 0)
+
+
+@pytest.mark.parametrize("B,N,H,Hkv,d,causal,mode", [
+    (3, 1000, 4, 2, 128, True, api.MODE_BLOCK_HADAMARD),
+    (5, 777, 2, 2, 64, False, api.MODE_BLOCK),
+    (2, 512, 2, 1, 256, True, api.MODE_BLOCK_HADAMARD),
+])
+def test_fp8_host_forward_matches_device_path(B, N, H, Hkv, d, causal, mode):
+    """attn_fwd_fp8_host = attn_fp8_prep of Q, K, V + attn_fwd_fp8 on the
+    device, bit for bit (block scales are per sequence, so chunking does not
+    change them)."""
+    q, k, v = host_qkv(B, N, H, Hkv, d, seed=300 + d)
+    o, lse = api.attn_fwd_fp8_host(q, k, v, mode=mode, sign_seed=99, causal=causal)
+    torch.cuda.synchronize()
+    dev = torch.device("cuda:0")
+    q8, k8, v8, qs, ks, vs = api.fp8_prepare_qkv(q.to(dev), k.to(dev), v.to(dev), mode, 99)
+    o_ref, lse_ref = api.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=causal)
+    torch.cuda.synchronize()
+    assert api.device_status() == (0, 0)
+    assert torch.equal(o.view(torch.int16), o_ref.cpu().view(torch.int16))
+    assert torch.equal(lse, lse_ref.cpu())
+
+
+def test_fp8_and_bf16_host_calls_interleave():
+    """FP8 and bf16 host calls of different layouts, in flight on two streams
+    with one shared workspace, each return their own device-path result."""
+    dev = torch.device("cuda:0")
+    B, N, H, d = 4, 640, 4, 128
+    ws = torch.empty(api.fwd_fp8_host_workspace_bytes(B, H, H, N, d), dtype=torch.uint8, device=dev)
+    streams = [torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)]
+    runs = []
+    for i in range(6):
+        q, k, v = host_qkv(B, N, H, H, d, seed=400 + i)
+        if i % 2:
+            res = api.attn_fwd_fp8_host(q, k, v, sign_seed=5, causal=True, workspace=ws, stream=streams[i % 2])
+        else:
+            res = api.attn_fwd_host(q, k, v, causal=True, workspace=ws, stream=streams[i % 2])
+        runs.append(((q, k, v), i, res))
+    torch.cuda.synchronize()
+    for (q, k, v), i, (o, lse) in runs:
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        if i % 2:
+            q8, k8, v8, qs, ks, vs = api.fp8_prepare_qkv(qd, kd, vd, api.MODE_BLOCK_HADAMARD, 5)
+            o_ref, lse_ref = api.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True)
+        else:
+            o_ref, lse_ref = api.attn_fwd(qd, kd, vd, causal=True)
+        assert torch.equal(o.view(torch.int16), o_ref.cpu().view(torch.int16)), i
+        assert torch.equal(lse, lse_ref.cpu()), i
+    assert api.device_status() == (0, 0)
