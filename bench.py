@@ -643,7 +643,7 @@ def main():
                                     "memory-bound launches around it (D / accumulator zeroing, dQ conversion)")
 
     if not args.quick and rank == 0:
-        line["e2e"] = e2e_measure(api, w, device, stream, arrs0, flops, steps=min(args.steps, 20))
+        line["e2e"] = e2e_measure(api, w, device, stream, arrs0, flops, steps=min(args.steps, 100))
         if w["dtype"] == "bf16" and args.workload == "c2":
             line["fp8"] = fp8_secondary(api, device, stream, steps=min(args.steps, 200))
             line["bwd"] = bwd_secondary(api, device, stream, steps=min(args.steps, 50))
@@ -766,37 +766,44 @@ def bwd_secondary(api, device, stream, steps):
 
 def e2e_measure_bwd(api, w, device, stream, arrs, flops, steps):
     """Backward end to end with HOST buffers: pinned Q, K, V, dO and the
-    forward's O, LSE copied in, attn_bwd, dQ, dK, dV copied back, all inside
-    the timed region."""
+    forward's O, LSE copied in, the backward, dQ, dK, dV copied back, all
+    inside the timed region (through attn_bwd_host)."""
     import torch
     host = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in arrs]
     hq, hk, hv, hdo = host
     dq_, dk_, dv_, ddo = (torch.empty_like(t, device=device) for t in host)
     o_dev, lse_dev = api.attn_fwd(dq_.copy_(hq), dk_.copy_(hk), dv_.copy_(hv), causal=w["causal"], window=w["window"])
     ho, hl = o_dev.cpu().pin_memory(), lse_dev.cpu().pin_memory()
-    do_dev, dl_dev = torch.empty_like(o_dev), torch.empty_like(lse_dev)
-    gq, gk, gv = torch.empty_like(dq_), torch.empty_like(dk_), torch.empty_like(dv_)
-    hgq, hgk, hgv = (torch.empty_like(t, device="cpu").pin_memory() for t in (gq, gk, gv))
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
-    work = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=device)
+    Hkv = hk.shape[2]
+    # The library's host-buffer backward: chunks of sequences staged through
+    # two device slots; consecutive steps alternate between two streams so
+    # that one step's copies overlap the previous step's backward.
+    ws = torch.empty(api.bwd_host_workspace_bytes(B, H, Hkv, N, d), dtype=torch.uint8, device=device)
+    outs = [tuple(torch.empty_like(t).pin_memory() for t in (hq, hk, hv)) for _ in range(2)]
+    streams = [stream, torch.cuda.Stream(device=device)]
+    turn = [0]
 
     def step():
-        with torch.cuda.stream(stream):
-            for dst, src in ((dq_, hq), (dk_, hk), (dv_, hv), (ddo, hdo), (do_dev, ho), (dl_dev, hl)):
-                dst.copy_(src, non_blocking=True)
-            api.attn_bwd(ddo, dq_, dk_, dv_, do_dev, dl_dev, causal=w["causal"], window=w["window"], dq=gq, dk=gk,
-                         dv=gv, workspace=work, stream=stream)
-            for dst, src in ((hgq, gq), (hgk, gk), (hgv, gv)):
-                dst.copy_(src, non_blocking=True)
+        i = turn[0] & 1
+        turn[0] += 1
+        gq, gk, gv = outs[i]
+        api.attn_bwd_host(hdo, hq, hk, hv, ho, hl, causal=w["causal"], window=w["window"], dq=gq, dk=gk, dv=gv,
+                          workspace=ws, stream=streams[i])
 
     for _ in range(3):
         step()
     torch.cuda.synchronize(device)
-    ms = time_loop(step, steps, stream) / steps
+    ms = time_loop_two_streams(step, steps, streams) / steps
+    hgq, hgk, hgv = outs[0]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, ho, hl))
     d2h = sum(t.numel() * t.element_size() for t in (hgq, hgk, hgv))
+    seqs_per_chunk = -(-B // min(B, 4))
     return {"value": round(flops / (ms / 1e3) / 1e12, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "kernel_launches_per_step": 3}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "kernel_launches_per_step": 3 * -(-B // seqs_per_chunk),
+            "api": "attn_bwd_host (pinned host buffers; per-sequence chunks, copies overlapped with the compute; "
+                   "two streams)"}
 
 
 def fp8_secondary(api, device, stream, steps):

@@ -74,6 +74,10 @@ def library() -> ctypes.CDLL:
         L.attn_fwd_fp8_host_workspace_size.restype = sz
         L.attn_fwd_fp8_host.argtypes = [P, P, P, P, P, i, i, i, i, i, i, f, i, i, u64, P, sz, P]
         L.attn_fwd_fp8_host.restype = i
+        L.attn_bwd_host_workspace_size.argtypes = [i, i, i, i, i]
+        L.attn_bwd_host_workspace_size.restype = sz
+        L.attn_bwd_host.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, f, i, P, sz, P]
+        L.attn_bwd_host.restype = i
         L.attn_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int)]
         L.attn_device_status.restype = i
         L.attn_set_wait_limit.argtypes = [u64]
@@ -246,6 +250,39 @@ def attn_fwd_sparse(q, k, v, block_mask, causal: bool = False, scale: float | No
                                    ctypes.c_void_p(_stream(stream)))
     _check("attn_fwd_sparse", rc)
     return out, lse
+
+
+def bwd_host_workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int) -> int:
+    return int(library().attn_bwd_host_workspace_size(B, H, H_kv, N, d))
+
+
+def attn_bwd_host(dout, q, k, v, out, lse, causal: bool = False, scale: float | None = None, window: int = 0,
+                  dq=None, dk=None, dv=None, workspace=None, device=None, stream=None):
+    """attn_bwd on HOST tensors (bf16 CPU q, dout, out (B, N, H, d); k, v
+    (B, N, H_kv, d); float32 lse (B, H, N)), staged through ``workspace`` (at
+    least bwd_host_workspace_bytes(...) bytes on ``device``) like
+    attn_fwd_host.  Returns host (dq, dk, dv); asynchronous on ``stream``."""
+    B, N, H, Hkv, d, _, _ = _host_args(q, k, v, out, lse)
+    if dout.is_cuda or dout.shape != q.shape or dout.dtype != torch.bfloat16 or not dout.is_contiguous():
+        raise ValueError("dout must be a contiguous bf16 CPU tensor shaped like q")
+    pin = q.is_pinned()
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=pin) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, pin_memory=pin) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, pin_memory=pin) if dv is None else dv
+    for t, ref in ((dq, q), (dk, k), (dv, v)):
+        if t.is_cuda or t.shape != ref.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("dq, dk, dv must be contiguous bf16 CPU tensors shaped like q, k, v")
+    device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if workspace is None:
+        workspace = torch.empty(max(bwd_host_workspace_bytes(B, H, Hkv, N, d), 256), dtype=torch.uint8,
+                                device=device)
+    with torch.cuda.device(workspace.device):
+        rc = library().attn_bwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                                     _ptr(dk), _ptr(dv), B, H, Hkv, N, d, int(bool(causal)), float(scale or 0.0),
+                                     int(window), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     ctypes.c_void_p(_stream(stream)))
+    _check("attn_bwd_host", rc)
+    return dq, dk, dv
 
 
 def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

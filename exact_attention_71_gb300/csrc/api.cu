@@ -542,41 +542,47 @@ int host_pipe(HostPipe** out) {
     return ATTN_OK;
 }
 
-// Staging layout of one slot: the chunk's inputs (Q, K, V), outputs (O,
-// LSE) and the scratch its compute step uses, each part 256-byte aligned.
+// Staging layout of one slot: the chunk's inputs, outputs and the scratch
+// its compute step uses, each part 256-byte aligned.  Part sizes are given
+// per sequence; the batch dimension is outermost in every host tensor.
 struct Staging {
     long long cb = 0;                  // sequences per chunk
-    size_t in_seq[3] = {}, out_seq[2] = {};
-    size_t in_off[3] = {}, out_off[2] = {}, scratch_off = 0, slot = 0;
+    int n_in = 0, n_out = 0;
+    size_t in_seq[6] = {}, out_seq[3] = {};
+    size_t in_off[6] = {}, out_off[3] = {}, scratch_off = 0, slot = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Q, K, V in and O, LSE out for (B, N, H / H_kv, d) bf16 tensors, plus
-// `scratch_per_seq` bytes of scratch parts (each rounded per chunk).
-bool staging(int B, int H, int H_kv, int N, int d, const size_t* scratch_per_seq, int n_scratch, Staging* L) {
-    if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return false;
+bool staging(int B, const size_t* in_seq, int n_in, const size_t* out_seq, int n_out, const size_t* scratch_seq,
+             int n_scratch, Staging* L) {
+    if (B <= 0) return false;
     const long long nch = B < kHostChunks ? B : kHostChunks;
     L->cb = (B + nch - 1) / nch;
     const size_t cb = static_cast<size_t>(L->cb);
-    const size_t q_seq = static_cast<size_t>(N) * H * d * 2, kv_seq = static_cast<size_t>(N) * H_kv * d * 2;
-    L->in_seq[0] = q_seq;
-    L->in_seq[1] = L->in_seq[2] = kv_seq;
-    L->out_seq[0] = q_seq;
-    L->out_seq[1] = static_cast<size_t>(H) * N * 4;
+    L->n_in = n_in;
+    L->n_out = n_out;
     size_t off = 0;
-    for (int x = 0; x < 3; ++x) { L->in_off[x] = off; off += up256(cb * L->in_seq[x]); }
-    for (int x = 0; x < 2; ++x) { L->out_off[x] = off; off += up256(cb * L->out_seq[x]); }
+    for (int x = 0; x < n_in; ++x) { L->in_seq[x] = in_seq[x]; L->in_off[x] = off; off += up256(cb * in_seq[x]); }
+    for (int x = 0; x < n_out; ++x) { L->out_seq[x] = out_seq[x]; L->out_off[x] = off; off += up256(cb * out_seq[x]); }
     L->scratch_off = off;
-    for (int x = 0; x < n_scratch; ++x) off += up256(cb * scratch_per_seq[x]);
+    for (int x = 0; x < n_scratch; ++x) off += up256(cb * scratch_seq[x]);
     L->slot = off;
     return true;
+}
+
+// The forward's parts: Q, K, V in; O, LSE out.
+bool fwd_staging(int B, int H, int H_kv, int N, int d, const size_t* scratch_seq, int n_scratch, Staging* L) {
+    if (H <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return false;
+    const size_t q_seq = static_cast<size_t>(N) * H * d * 2, kv_seq = static_cast<size_t>(N) * H_kv * d * 2;
+    const size_t in[3] = {q_seq, kv_seq, kv_seq}, out[2] = {q_seq, static_cast<size_t>(H) * N * 4};
+    return staging(B, in, 3, out, 2, scratch_seq, n_scratch, L);
 }
 
 // Runs the chunks of one call through the staging slots (see above).
 // compute(nb, slot_base, stream) queues the chunk's work on `stream`.
 template <class Compute>
-int host_pipeline(const void* const in[3], void* const out[2], int B, const Staging& L, void* workspace,
+int host_pipeline(const void* const* in, void* const* out, int B, const Staging& L, void* workspace,
                   size_t workspace_bytes, void* stream, const char* who, Compute&& compute) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < 2 * L.slot)
         return fail(ATTN_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned and at least %zu bytes (got %zu)",
@@ -604,7 +610,7 @@ int host_pipeline(const void* const in[3], void* const out[2], int B, const Stag
         ++P->chunks;
         char* base = static_cast<char*>(workspace) + slot * L.slot;
         e = cudaStreamWaitEvent(P->h2d, P->freed[slot], 0);
-        for (int x = 0; x < 3 && e == cudaSuccess; ++x)
+        for (int x = 0; x < L.n_in && e == cudaSuccess; ++x)
             e = cudaMemcpyAsync(base + L.in_off[x], static_cast<const char*>(in[x]) + b0 * L.in_seq[x],
                                 nb * L.in_seq[x], cudaMemcpyHostToDevice, P->h2d);
         if (e == cudaSuccess) e = cudaEventRecord(P->loaded[slot], P->h2d);
@@ -617,7 +623,7 @@ int host_pipeline(const void* const in[3], void* const out[2], int B, const Stag
         if (rc != ATTN_OK) break;
         e = cudaEventRecord(P->computed[slot], P->comp);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(P->d2h, P->computed[slot], 0);
-        for (int x = 0; x < 2 && e == cudaSuccess; ++x)
+        for (int x = 0; x < L.n_out && e == cudaSuccess; ++x)
             e = cudaMemcpyAsync(static_cast<char*>(out[x]) + b0 * L.out_seq[x], base + L.out_off[x],
                                 nb * L.out_seq[x], cudaMemcpyDeviceToHost, P->d2h);
         if (e == cudaSuccess) e = cudaEventRecord(P->freed[slot], P->d2h);
@@ -646,7 +652,7 @@ extern "C" {
 
 size_t attn_fwd_host_workspace_size(int B, int H, int H_kv, int N, int d) {
     Staging L;
-    if (!staging(B, H, H_kv, N, d, nullptr, 0, &L)) return 0;
+    if (!fwd_staging(B, H, H_kv, N, d, nullptr, 0, &L)) return 0;
     return 2 * L.slot;
 }
 
@@ -660,7 +666,7 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
         return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
     if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
     Staging L;
-    staging(B, H, H_kv, N, d, nullptr, 0, &L);
+    fwd_staging(B, H, H_kv, N, d, nullptr, 0, &L);
     const void* in[3] = {q, k, v};
     void* out[2] = {o, lse};
     return host_pipeline(in, out, B, L, workspace, workspace_bytes, stream, "attn_fwd_host",
@@ -677,7 +683,7 @@ size_t attn_fwd_fp8_host_workspace_size(int B, int H, int H_kv, int N, int d) {
     size_t sc[6];
     if (H <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return 0;
     fp8_scratch(H, H_kv, N, d, sc);
-    if (!staging(B, H, H_kv, N, d, sc, 6, &L)) return 0;
+    if (!fwd_staging(B, H, H_kv, N, d, sc, 6, &L)) return 0;
     return 2 * L.slot;
 }
 
@@ -696,7 +702,7 @@ int attn_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, floa
     Staging L;
     size_t sc[6];
     fp8_scratch(H, H_kv, N, d, sc);
-    staging(B, H, H_kv, N, d, sc, 6, &L);
+    fwd_staging(B, H, H_kv, N, d, sc, 6, &L);
     size_t soff[6];
     for (int x = 0; x < 6; ++x)
         soff[x] = x == 0 ? L.scratch_off : soff[x - 1] + up256(static_cast<size_t>(L.cb) * sc[x - 1]);
@@ -719,6 +725,61 @@ int attn_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, floa
                              return launch_forward(true, base + soff[0], base + soff[1], base + soff[2],
                                                    base + L.out_off[0], reinterpret_cast<float*>(base + L.out_off[1]),
                                                    nb, H, H_kv, N, d, causal, scale, window, qs, ks, vs, s);
+                         });
+}
+
+}  // extern "C"
+
+namespace {
+
+// The backward's parts: Q, K, V, O, LSE, dO in; dQ, dK, dV out; the
+// backward's own workspace for one chunk as scratch.
+bool bwd_staging(int B, int H, int H_kv, int N, int d, Staging* L) {
+    if (B <= 0 || H <= 0 || H_kv <= 0 || N <= 0 || d <= 0) return false;
+    const size_t q_seq = static_cast<size_t>(N) * H * d * 2, kv_seq = static_cast<size_t>(N) * H_kv * d * 2;
+    const size_t l_seq = static_cast<size_t>(H) * N * 4;
+    const size_t in[6] = {q_seq, kv_seq, kv_seq, q_seq, l_seq, q_seq}, out[3] = {q_seq, kv_seq, kv_seq};
+    if (!staging(B, in, 6, out, 3, nullptr, 0, L)) return false;
+    // one chunk's backward workspace (not a per-sequence size: added whole)
+    L->slot += up256(static_cast<size_t>(attn::bwd_workspace(static_cast<int>(L->cb), H, N, d).bytes));
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t attn_bwd_host_workspace_size(int B, int H, int H_kv, int N, int d) {
+    Staging L;
+    if (!bwd_staging(B, H, H_kv, N, d, &L)) return 0;
+    return 2 * L.slot;
+}
+
+int attn_bwd_host(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int d, int causal, float scale,
+                  int window, void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = '\0';
+    int rc = check_common(q, k, v, o, lse, B, H, N, d, window);
+    if (rc != ATTN_OK) return rc;
+    if (d != 128 && d != 64) return fail(ATTN_ERR_UNSUPPORTED, "attn_bwd_host supports head_dim 64 and 128 (got %d)", d);
+    if (H_kv <= 0 || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    if (!dout || !dq || !dk || !dv) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    Staging L;
+    bwd_staging(B, H, H_kv, N, d, &L);
+    const size_t bwd_ws = up256(static_cast<size_t>(attn::bwd_workspace(static_cast<int>(L.cb), H, N, d).bytes));
+    const void* in[6] = {q, k, v, o, lse, dout};
+    void* out[3] = {dq, dk, dv};
+    return host_pipeline(in, out, B, L, workspace, workspace_bytes, stream, "attn_bwd_host",
+                         [&](int nb, char* base, cudaStream_t s) {
+                             return attn_bwd(base + L.in_off[0], base + L.in_off[1], base + L.in_off[2],
+                                             base + L.in_off[3], reinterpret_cast<const float*>(base + L.in_off[4]),
+                                             base + L.in_off[5], base + L.out_off[0], base + L.out_off[1],
+                                             base + L.out_off[2], base + L.scratch_off, bwd_ws, nb, H, H_kv, N, d,
+                                             causal, scale, window, s);
                          });
 }
 

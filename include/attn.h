@@ -266,6 +266,24 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              float scale, int window, void* stream);
 
 /*
+ * attn_bwd_host_workspace_size / attn_bwd_host -- attn_bwd on HOST buffers
+ * (no counterpart in the pages): per chunk of whole sequences, q, k, v, o,
+ * lse and dout are copied to a device staging slot, the backward runs there
+ * (its scratch is part of the slot) and dq, dk, dv are copied back, staged
+ * and overlapped exactly as attn_fwd_host.
+ *   q, k, v, o, lse, dout : HOST inputs with the layouts of attn_bwd
+ *   dq, dk, dv            : HOST outputs, written
+ *   workspace             : device, at least attn_bwd_host_workspace_size(B,
+ *                           H, H_kv, N, d) bytes, 256-byte aligned
+ * d must be 64 or 128.  Ordering, sharing and errors as attn_fwd_host.
+ */
+size_t attn_bwd_host_workspace_size(int B, int H, int H_kv, int N, int d);
+int attn_bwd_host(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N,
+                  int d, int causal, float scale, int window, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_noalloc / attn_bwd_noalloc_max_scratch -- attn_bwd for callers
  * that cannot allocate device memory: code running where cudaMalloc is not
  * allowed or not wanted (inside a framework's own allocator or memory pool,

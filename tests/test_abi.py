@@ -171,3 +171,21 @@ def test_fp8_host_forward_workspace_and_arguments(lib):
     assert b"mode" in lib.attn_last_error_string()
     assert f(*args(d=96)) == -2
     assert f(*args(wsb=ws - 1)) == -1
+
+
+def test_bwd_host_workspace_and_arguments(lib):
+    """attn_bwd_host: per slot Q, K, V, O, LSE, dO in and dQ, dK, dV out for
+    one chunk, plus that chunk's backward workspace."""
+    size = lib.attn_bwd_host_workspace_size
+    up = lambda x: (x + 255) // 256 * 256
+    B, H, Hkv, N, d = 3, 2, 1, 100, 128
+    q_seq, kv_seq, l_seq = N * H * d * 2, N * Hkv * d * 2, H * N * 4
+    parts = [q_seq, kv_seq, kv_seq, q_seq, l_seq, q_seq, q_seq, kv_seq, kv_seq]
+    slot = sum(up(x) for x in parts) + up(lib.attn_bwd_workspace_size(1, H, N, d))
+    assert size(B, H, Hkv, N, d) == 2 * slot
+    assert size(B, H, 0, N, d) == 0
+    f = lib.attn_bwd_host
+    ws = size(B, H, Hkv, N, d)
+    args = lambda d=128, wsb=ws: (FAKE,) * 9 + (B, H, Hkv, N, d, 1, 0.0, 0, FAKE, wsb, None)
+    assert f(*args(d=256)) == -2
+    assert f(*args(wsb=ws - 1)) == -1

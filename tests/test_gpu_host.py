@@ -138,3 +138,30 @@ def test_fp8_and_bf16_host_calls_interleave():
         assert torch.equal(o.view(torch.int16), o_ref.cpu().view(torch.int16)), i
         assert torch.equal(lse, lse_ref.cpu()), i
     assert api.device_status() == (0, 0)
+
+
+@pytest.mark.parametrize("B,N,H,Hkv,d,causal", [(3, 700, 4, 2, 128, True), (5, 384, 2, 2, 64, False)])
+def test_bwd_host_matches_device_backward(B, N, H, Hkv, d, causal):
+    """attn_bwd_host = attn_bwd on the device: dK and dV bit for bit (one CTA
+    owns each key block); dQ up to the order of its float32 accumulation
+    (bulk adds from several CTAs), checked against the oracle as well."""
+    dev = torch.device("cuda:0")
+    q, k, v = host_qkv(B, N, H, Hkv, d, seed=500 + d)
+    do = torch.from_numpy(synth.tensor_bf16((B, N, H, d), seed=500 + d, stream=4).view(np.int16)).view(
+        torch.bfloat16).pin_memory()
+    o_d, lse_d = api.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=causal)
+    o, lse = o_d.cpu().pin_memory(), lse_d.cpu().pin_memory()
+    dq, dk, dv = api.attn_bwd_host(do, q, k, v, o, lse, causal=causal)
+    torch.cuda.synchronize()
+    rq, rk, rv = api.attn_bwd(do.to(dev), q.to(dev), k.to(dev), v.to(dev), o_d, lse_d, causal=causal)
+    torch.cuda.synchronize()
+    assert api.device_status() == (0, 0)
+    assert torch.equal(dk.view(torch.int16), rk.cpu().view(torch.int16))
+    assert torch.equal(dv.view(torch.int16), rv.cpu().view(torch.int16))
+    diff = (dq.float() - rq.cpu().float()).abs().max().item()
+    assert diff <= 2e-2 * rq.float().abs().max().item()
+    as_np = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    refs = oracle.attention_bwd(as_np(q), as_np(k), as_np(v), as_np(do), causal=causal)
+    for g, r in zip((dq, dk, dv), refs):
+        g = g.float().double().numpy()
+        assert np.linalg.norm(g - r) / np.linalg.norm(r) <= 5e-3
