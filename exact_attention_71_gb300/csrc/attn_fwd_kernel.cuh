@@ -102,7 +102,7 @@ struct FwdCfg {
     // Issuer warps: one per query tile where the tile's MMAs are long enough
     // (bf16, d = 128) for the hand-off latency to dominate; one warp for both
     // tiles where the softmax is the longer phase (FP8, d = 64) or NQ = 1.
-    static constexpr int MMA_WARPS = (!FP8 && !SPARSE && D == 128 && NQ == 2) ? 2 : 1;
+    static constexpr int MMA_WARPS = (!FP8 && D == 128 && NQ == 2) ? 2 : 1;
     static constexpr int THREADS = NQ * 128 + 128;
     static constexpr int BAR_BYTES = 256;
     // The reference maximum of a row moves only when the row maximum exceeds
@@ -316,10 +316,15 @@ __device__ __forceinline__ WorkItem<Cfg::NQ> decode_item(const FwdParams& p, int
     return w;
 }
 
-// MMA issue order of an item (the ping-pong of the two query tiles): for
-// u = u_lo .. u_hi + 1 and t = 0, 1 the block (t, u) holds O_t += P_t V_{u-1}
-// (when key tile u-1 is in tile t's range) and S_t = Q_t K_u^T (when u is);
-// empty blocks are skipped.  Returns the number of blocks before (t, u).
+// MMA issue order (the ping-pong of the two query tiles): an item's steps
+// u = u_lo .. (its last key tile) + 1 in walk order and, within a step, t =
+// 0, 1; the block (t, u) holds O_t += P_t V_{u-1} (when key tile u-1 is in
+// tile t's set) and S_t = Q_t K_u^T (when u is); empty blocks are skipped.
+// With two issuers each waits for its blocks' turns in this order.  Dense
+// walks are contiguous, so a block's position has a closed form
+// (blocks_before, plus the blocks of the CTA's earlier items); sparse walks
+// are not, so there both issuers walk every step and count every non-empty
+// block (a running count across items).
 template <int NQ>
 __device__ __forceinline__ int blocks_before(const WorkItem<NQ>& w, int t, int u) {
     int n = 0;
@@ -541,7 +546,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         uint32_t pv_count[NQ], qn[NQ];
 #pragma unroll
         for (int t = 0; t < NQ; ++t) pv_count[t] = qn[t] = 0;
-        int item_base = 0;
+        int item_base = 0;   // dense: blocks of the CTA's earlier items
+        int turn = 0;        // sparse: non-empty blocks (of both issuers) so far
         bool ok = true;
         for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
             const int item = round_item(rnd);
@@ -569,17 +575,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 bool issued_any = false;
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
-                    if (t % MW != wi || !w.active[t]) continue;
+                    if (!w.active[t]) continue;
+                    if (!Cfg::SPARSE && t % MW != wi) continue;
                     const bool do_pv = prev >= 0 && key_in_tile<Cfg>(w, t, prev);
                     const bool do_s = u >= 0 && key_in_tile<Cfg>(w, t, u);
                     if (!do_pv && !do_s) continue;
+                    int k;
+                    if constexpr (Cfg::SPARSE) {
+                        k = turn++;
+                        if (t % MW != wi) continue;
+                    } else {
+                        // (the final step of a dense walk is u_hi + 1)
+                        k = item_base + blocks_before(w, t, u >= 0 ? u : prev + 1);
+                    }
                     if (do_pv && !warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
                         ok = false;
                         break;
                     }
-                    // (the turn counter is used by the dense instantiations only,
-                    // whose walk is contiguous: the final step is u_hi + 1)
-                    const int k = item_base + blocks_before(w, t, u >= 0 ? u : prev + 1);
                     if (MW > 1 && !wait_turn(issued, k, abort_flag, p, SITE_TURN)) {
                         ok = false;
                         break;
