@@ -12,16 +12,13 @@
 // back (§3.2's overlap of one iteration's GEMM with the next one's softmax,
 // S_BUFS - 1 iterations deep).
 //
-// Roles (one CTA per SM):
-//   warps [0, 4*HALVES)  softmax; warp w serves TMEM lanes 32 (w % 4) .. +31
-//                        (one query row per thread) and key columns
-//                        [COLS (w / 4), COLS (w / 4) + COLS) of every S tile.
-//                        With HALVES = 2 the two warps of a row exchange their
-//                        row maxima (and at the end their row sums) through
-//                        shared memory.
-//   warp 4*HALVES        TMA producer: Q, then ring stages {K(i), V(i - S_BUFS)}
-//   warp 4*HALVES + 1    MMA issuer: per stage, O += P(i - S_BUFS) V, then
-//                        S(i) = Q K(i)^T into buffer i % S_BUFS
+// Roles (one CTA per SM, 256 threads):
+//   warps 0-3   softmax; warp w serves TMEM lanes 32 w .. +31 (one query row
+//               per thread)
+//   warp 4      TMA producer: Q, then ring stages {K(i), V(i - S_BUFS)}
+//   warp 5      MMA issuer: per stage, O += P(i - S_BUFS) V, then
+//               S(i) = Q K(i)^T into buffer i % S_BUFS
+//   warps 6-7   idle
 // Tensor memory: S buffers at columns BN b (b < S_BUFS), P(i) over the first
 // columns of its S buffer, O at columns BN S_BUFS .. + D.
 //
@@ -31,42 +28,26 @@
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
-#include "sm103_bulk.cuh"
 
 namespace attn {
 
-template <int D_, int BN_, bool FP8_, int HALVES_, int S_BUFS_, bool SPARSE_ = false>
+template <int D_, int BN_, bool FP8_, int S_BUFS_, bool SPARSE_ = false>
 struct LaCfg : FwdCfg<D_, BN_, 1, FP8_, SPARSE_> {
     using Base = FwdCfg<D_, BN_, 1, FP8_, SPARSE_>;
-    static constexpr int HALVES = HALVES_;      // softmax warpgroups per row (key columns split)
     static constexpr int S_BUFS = S_BUFS_;      // S buffers in tensor memory
-    static constexpr int COLS = Base::BN / HALVES;   // key columns per softmax thread
-    static constexpr int DH = Base::D / HALVES;      // O columns per softmax thread
-    static constexpr int SOFTMAX_WARPS = 4 * HALVES;
-    static constexpr int LOAD_WARP = SOFTMAX_WARPS;
-    static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;
+    static constexpr int SOFTMAX_WARPS = 4;
+    static constexpr int LOAD_WARP = 4;
+    static constexpr int MMA_WARP = 5;
     static constexpr int MMA_WARPS = 1;
-    static constexpr int THREADS = SOFTMAX_WARPS * 32 + 128;
+    // 256 threads: every warp keeps the launch allocation (no register split).
+    static constexpr int THREADS = 256;
     static constexpr int S_STRIDE = BN_;          // TMEM columns per S buffer
     static constexpr int O_COL0 = S_STRIDE * S_BUFS;
-    // Shared memory: Q, the ring, barriers, then the row-max / row-sum
-    // exchange ([2 parities][HALVES][128] + [HALVES][128] floats).
-    static constexpr int XCH_BYTES = 3 * HALVES * 128 * 4;
-    static constexpr int SMEM_BYTES = 1024 + Base::Q_TILE_BYTES + Base::NSTAGE * Base::STAGE_BYTES +
-                                      Base::BAR_BYTES + XCH_BYTES;
-    static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 248 : (65536 / THREADS) / 8 * 8;
-    // With one softmax warpgroup (256 threads) every warp can keep the launch
-    // allocation; with two, the load / MMA warpgroup gives registers to the
-    // softmax warpgroups (setmaxnreg).
-    static constexpr bool REG_SPLIT = HALVES == 2;
-    static constexpr int LOW_REGS = 72;
-    static constexpr int HIGH_REGS_RAW = ((LAUNCH_REGS * THREADS - LOW_REGS * 128) / (SOFTMAX_WARPS * 32)) / 8 * 8;
-    static constexpr int HIGH_REGS = HIGH_REGS_RAW > 248 ? 248 : HIGH_REGS_RAW;
-    static_assert(HIGH_REGS * SOFTMAX_WARPS * 32 + LOW_REGS * 128 <= LAUNCH_REGS * THREADS, "register split");
-    static_assert(HALVES == 1 || HALVES == 2, "halves");
+    static constexpr int SMEM_BYTES = 1024 + Base::Q_TILE_BYTES + Base::NSTAGE * Base::STAGE_BYTES + Base::BAR_BYTES;
     static_assert(O_COL0 + D_ <= 512, "tensor memory budget");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-    static_assert(COLS % (FP8_ ? 64 : 32) == 0 && DH % 32 == 0, "column split");
+    static_assert(S_BUFS >= 2 && S_BUFS <= 4, "S buffers");
+    static_assert(BN_ % (FP8_ ? 64 : 32) == 0, "key tile");
 };
 
 struct LaBarriers {
@@ -84,14 +65,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     attn_fwd_la_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                        const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
     constexpr int D = Cfg::D, BN = Cfg::BN, BM = Cfg::BM, NSTAGE = Cfg::NSTAGE;
-    constexpr int HALVES = Cfg::HALVES, L = Cfg::S_BUFS, COLS = Cfg::COLS, DH = Cfg::DH;
+    constexpr int L = Cfg::S_BUFS;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
     uint8_t* sKV = smem + Cfg::Q_TILE_BYTES;                    // NSTAGE x {K tile, V tile}
     LaBarriers* bars = reinterpret_cast<LaBarriers*>(sKV + NSTAGE * Cfg::STAGE_BYTES);
-    float* xch = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + Cfg::BAR_BYTES);
     volatile int* abort_flag = &bars->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -131,7 +111,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int total_items = p.n_mblocks * p.B * p.H;
 
     if (warp >= Cfg::SOFTMAX_WARPS) {
-    if constexpr (Cfg::REG_SPLIT) regs_decrease<Cfg::LOW_REGS>();
     if (warp == Cfg::LOAD_WARP) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -276,18 +255,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         __syncwarp();
     }
     } else {
-        if constexpr (Cfg::REG_SPLIT) regs_increase<Cfg::HIGH_REGS>();
         // ------------------------------------------------------------ softmax
-        const int quad = warp & 3;
-        const int hf = warp >> 2;                 // key-column half (0 when HALVES = 1)
-        const int r = quad * 32 + lane;           // query row within the tile
-        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t s_base = tmem + lane_off + hf * COLS;
-        const uint32_t p_base = tmem + lane_off + hf * (COLS * Cfg::ES / 4);
-        const uint32_t o_tmem = tmem + lane_off + Cfg::O_COL0 + hf * DH;
-        float* xmax = xch;                        // [2][HALVES][128]
-        float* xsum = xch + 2 * HALVES * 128;     // [HALVES][128]
-        const uint32_t pair_bar = 1 + quad;       // named barrier of the two warps of these rows
+        const int r = warp * 32 + lane;           // query row within the tile
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t s_base = tmem + lane_off;  // P(i) goes over the first columns of S(i)
+        const uint32_t o_tmem = tmem + lane_off + Cfg::O_COL0;
         const int nblk = (p.N + 127) / 128;
         uint32_t s_cnt = 0, qn = 0, pv_seen = 0;
         bool ok = true;
@@ -301,14 +273,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (!tk.in_n) continue;
             const int i = qs + r;
             __nv_bfloat16* orow =
-                reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * p.N + i) * p.H + h) * D + hf * DH;
+                reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * p.N + i) * p.H + h) * D;
             if (!tk.active) {
                 // Block-sparse mask: this query tile sees no key.
                 if (i < p.N) {
                     uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-                    for (int x = 0; x < DH / 8; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
-                    if (hf == 0) p.lse[static_cast<size_t>(bh) * p.N + i] = -INFINITY;
+                    for (int x = 0; x < D / 8; ++x) dst[x] = make_uint4(0u, 0u, 0u, 0u);
+                    p.lse[static_cast<size_t>(bh) * p.N + i] = -INFINITY;
                 }
                 continue;
             }
@@ -329,17 +301,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             bool first_tile = true;
             for (int j = tk.first; j >= 0; j = next_in<Cfg>(tk, j)) {
                 const uint32_t sb = s_cnt % L;
-                bool wt = wait_phase(&bars->s_full[sb], (s_cnt / L) & 1, abort_flag, p, SITE_SOFTMAX_S);
-                wt = __all_sync(0xffffffffu, wt);
-                uint32_t sr[COLS];
-                if (wt) {
-                    tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < COLS / 32; ++c) tmem_ld32(s_base + sb * Cfg::S_STRIDE + c * 32, sr + c * 32);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < COLS / 32; ++c) reg_fence32(sr + c * 32);
+                const bool wt = wait_phase(&bars->s_full[sb], (s_cnt / L) & 1, abort_flag, p, SITE_SOFTMAX_S);
+                if (!__all_sync(0xffffffffu, wt)) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after();
+                uint32_t sr[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_base + sb * Cfg::S_STRIDE + c * 32, sr + c * 32);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) reg_fence32(sr + c * 32);
                 float mult = q_mult;
                 float pv_mult = 1.0f;
                 if constexpr (Cfg::FP8) {
@@ -347,10 +320,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     mult *= p.k_scale[sbk];
                     pv_mult = Cfg::P8_SCALE * (p.v_scale[sbk] / vmax);
                 }
-                const int kbase = j * BN + hf * COLS;
-                if (kbase < klo || kbase + COLS - 1 > khi) {
+                const int kbase = j * BN;
+                if (kbase < klo || kbase + BN - 1 > khi) {
 #pragma unroll
-                    for (int c = 0; c < COLS; ++c) {
+                    for (int c = 0; c < BN; ++c) {
                         const int key = kbase + c;
                         if (key < klo || key > khi) sr[c] = __float_as_uint(-INFINITY);
                     }
@@ -358,26 +331,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
                 float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
 #pragma unroll
-                for (int c = 4; c + 8 <= COLS; c += 8) {
+                for (int c = 4; c + 8 <= BN; c += 8) {
                     mx0 = fmax3(mx0, __uint_as_float(sr[c + 0]), __uint_as_float(sr[c + 1]));
                     mx1 = fmax3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
                     mx2 = fmax3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
                     mx3 = fmax3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
                 }
-                mx0 = fmax3(mx0, mx1, __uint_as_float(sr[COLS - 4]));
-                mx2 = fmax3(mx2, mx3, __uint_as_float(sr[COLS - 3]));
-                float mx = fmax3(mx0, mx2, fmaxf(__uint_as_float(sr[COLS - 2]), __uint_as_float(sr[COLS - 1])));
-                if constexpr (HALVES == 2) {
-                    // Both warps of these rows have read their half of S(j)
-                    // once they pass this barrier, so P may then overwrite it.
-                    xmax[((s_cnt & 1) * 2 + hf) * 128 + r] = mx;
-                    ok = named_barrier_and(pair_bar, 64, wt);
-                    if (!ok) break;
-                    mx = fmaxf(mx, xmax[((s_cnt & 1) * 2 + (hf ^ 1)) * 128 + r]);
-                } else {
-                    ok = wt;
-                    if (!ok) break;
-                }
+                mx0 = fmax3(mx0, mx1, __uint_as_float(sr[BN - 4]));
+                mx2 = fmax3(mx2, mx3, __uint_as_float(sr[BN - 3]));
+                const float mx = fmax3(mx0, mx2, fmaxf(__uint_as_float(sr[BN - 2]), __uint_as_float(sr[BN - 1])));
                 const float m_tile = mx * mult;
                 float m_new = m;
                 if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY) m_new = fmaxf(m, m_tile);
@@ -385,11 +347,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const float alpha = ex2_approx(m - m_use);
                 const float2 mult2 = make_float2(mult, mult);
                 float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
-                const uint32_t p_tm = p_base + sb * Cfg::S_STRIDE;
+                const uint32_t p_tm = s_base + sb * Cfg::S_STRIDE;
                 if constexpr (!Cfg::FP8) {
                     const float2 neg2 = make_float2(-m_use, -m_use);
 #pragma unroll
-                    for (int c = 0; c < COLS / 32; ++c) {
+                    for (int c = 0; c < BN / 32; ++c) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int x = 0; x < 16; ++x) {
@@ -410,7 +372,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const float lg = __log2f(pv_mult);
                     const float2 negs = make_float2(-m_use + lg, -m_use + lg);
 #pragma unroll
-                    for (int c = 0; c < COLS / 64; ++c) {
+                    for (int c = 0; c < BN / 64; ++c) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int x = 0; x < 16; ++x) {
@@ -442,7 +404,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tc_fence_after();
                     if (__all_sync(0xffffffffu, wp) && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
-                        for (int c = 0; c < DH / 32; ++c) {
+                        for (int c = 0; c < D / 32; ++c) {
                             uint32_t orr[32];
                             tmem_ld32(o_tmem + c * 32, orr);
                             tmem_wait_ld();
@@ -465,23 +427,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (!ok) break;
             bool wt = wait_phase(&bars->o_full, qn & 1, abort_flag, p, SITE_SOFTMAX_O);
             ++qn;
-            wt = __all_sync(0xffffffffu, wt);
-            if constexpr (HALVES == 2) {
-                xsum[hf * 128 + r] = l;
-                ok = named_barrier_and(pair_bar, 64, wt);
-                if (!ok) break;
-                l += xsum[(hf ^ 1) * 128 + r];
-            } else {
-                ok = wt;
-                if (!ok) break;
-            }
+            ok = __all_sync(0xffffffffu, wt);
+            if (!ok) break;
             tc_fence_after();
             // l = 0 only for a row that sees no key: O = 0, LSE = -inf.
             float out_mult = l > 0.0f ? 1.0f / l : 0.0f;
             if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / Cfg::P8_SCALE);
             const bool store = i < p.N;
 #pragma unroll
-            for (int c = 0; c < DH / 32; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
                 uint32_t orr[32];
                 tmem_ld32(o_tmem + c * 32, orr);
                 tmem_wait_ld();
@@ -497,7 +451,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     for (int x = 0; x < 4; ++x) dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
                 }
             }
-            if (store && hf == 0) p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.69314718055994530942f;
+            if (store) p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.69314718055994530942f;
         }
     }
 
@@ -514,16 +468,7 @@ template <class Cfg>
 cudaError_t launch_fwd_la(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const FwdParams& p,
                           int max_ctas, cudaStream_t stream) {
     auto kernel = attn_fwd_la_kernel<Cfg>;
-    // The register split (setmaxnreg), where used, assumes LAUNCH_REGS
-    // registers per thread; a build with another count is refused.
-    cudaError_t e;
-    if constexpr (Cfg::REG_SPLIT) {
-        cudaFuncAttributes attr;
-        e = cudaFuncGetAttributes(&attr, kernel);
-        if (e != cudaSuccess) return e;
-        if (attr.numRegs != Cfg::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-    }
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const long long units = static_cast<long long>(p.n_mblocks) * p.B * p.H;
     const long long grid = units < max_ctas ? units : max_ctas;

@@ -5,7 +5,7 @@
 #include "attn_launch.cuh"
 
 namespace attn {
-using Cfg_fp8_d256 = LaCfg<256, 128, true, 1, 2>;
+using Cfg_fp8_d256 = LaCfg<256, 128, true, 2>;
 cudaError_t run_fwd_fp8_d256(const FwdMaps& m, const FwdParams& p, int g, cudaStream_t s) {
     return launch_fwd_la<Cfg_fp8_d256>(m.q, m.k, m.v, p, g, s);
 }

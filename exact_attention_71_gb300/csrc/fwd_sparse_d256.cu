@@ -5,7 +5,7 @@
 #include "attn_launch.cuh"
 
 namespace attn {
-using Cfg_sparse_d256 = LaCfg<256, 64, false, 1, 3, true>;
+using Cfg_sparse_d256 = LaCfg<256, 64, false, 3, true>;
 cudaError_t run_fwd_sparse_d256(const FwdMaps& m, const FwdParams& p, int g, cudaStream_t s) {
     return launch_fwd_la<Cfg_sparse_d256>(m.q, m.k, m.v, p, g, s);
 }
