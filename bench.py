@@ -382,8 +382,12 @@ def cpu_baseline(w, budget_s=12.0, arrs=None):
     arrs = _oracle_inputs(w, arrs)
     cores = os.cpu_count() or 1
     _, t, flops, desc = _oracle_size(w, arrs, budget_s, cores)
-    return {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-            "sample": desc + f", {t:.1f} s"}
+    out = {"value": flops / t / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+           "sample": desc + f", {t:.1f} s"}
+    # The same oracle on one core, on a smaller sample (a per-core figure).
+    _, t1, flops1, desc1 = _oracle_size(w, arrs, budget_s / 4, 1)
+    out["one_core"] = {"value": flops1 / t1 / 1e12, "unit": "TFLOPS", "sample": desc1 + f", {t1:.1f} s"}
+    return out
 
 
 def run_reference(args, w, key):
