@@ -102,6 +102,23 @@ def _stream(stream) -> int:
     return int(stream)
 
 
+def _torch_stream(stream, device):
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
+def _hold_until_done(t, stream):
+    """A workspace allocated here is still in use after this function
+    returns, by work on `stream` or (host-buffer entries) on the library's
+    own streams, which `stream` waits for; recording the tensor on `stream`
+    keeps torch's caching allocator from handing the memory out again before
+    that work is done."""
+    t.record_stream(_torch_stream(stream, t.device))
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
@@ -173,7 +190,8 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, win
     B, N, H, Hkv, d, out, lse = _host_args(q, k, v, out, lse)
     device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     need = fwd_host_workspace_bytes(B, H, Hkv, N, d)
-    if workspace is None:
+    own = workspace is None
+    if own:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
     with torch.cuda.device(workspace.device):
         rc = library().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N, d,
@@ -181,6 +199,8 @@ def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, win
                                      workspace.numel() * workspace.element_size(),
                                      ctypes.c_void_p(_stream(stream)))
     _check("attn_fwd_host", rc)
+    if own:
+        _hold_until_done(workspace, stream)
     return out, lse
 
 
@@ -216,7 +236,8 @@ def attn_fwd_fp8_host(q, k, v, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int =
     MODE_BLOCK_HADAMARD.  Returns host (O, LSE); asynchronous on ``stream``."""
     B, N, H, Hkv, d, out, lse = _host_args(q, k, v, out, lse)
     device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    if workspace is None:
+    own = workspace is None
+    if own:
         need = fwd_fp8_host_workspace_bytes(B, H, Hkv, N, d)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
     with torch.cuda.device(workspace.device):
@@ -226,6 +247,8 @@ def attn_fwd_fp8_host(q, k, v, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int =
                                          workspace.numel() * workspace.element_size(),
                                          ctypes.c_void_p(_stream(stream)))
     _check("attn_fwd_fp8_host", rc)
+    if own:
+        _hold_until_done(workspace, stream)
     return out, lse
 
 
@@ -273,7 +296,8 @@ def attn_bwd_host(dout, q, k, v, out, lse, causal: bool = False, scale: float | 
         if t.is_cuda or t.shape != ref.shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
             raise ValueError("dq, dk, dv must be contiguous bf16 CPU tensors shaped like q, k, v")
     device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-    if workspace is None:
+    own = workspace is None
+    if own:
         workspace = torch.empty(max(bwd_host_workspace_bytes(B, H, Hkv, N, d), 256), dtype=torch.uint8,
                                 device=device)
     with torch.cuda.device(workspace.device):
@@ -282,6 +306,8 @@ def attn_bwd_host(dout, q, k, v, out, lse, causal: bool = False, scale: float | 
                                      int(window), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      ctypes.c_void_p(_stream(stream)))
     _check("attn_bwd_host", rc)
+    if own:
+        _hold_until_done(workspace, stream)
     return dq, dk, dv
 
 
@@ -310,12 +336,15 @@ def attn_bwd(dout, q, k, v, out, lse, causal: bool = False, scale: float | None 
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     need = bwd_workspace_bytes(B, H, N, d)
-    if workspace is None:
+    own = workspace is None
+    if own:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     rc = library().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                             _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), B, H, Hkv, N, d,
                             int(bool(causal)), float(scale or 0.0), int(window), ctypes.c_void_p(_stream(stream)))
     _check("attn_bwd", rc)
+    if own and stream is not None:
+        _hold_until_done(workspace, stream)   # the launches run on `stream`, not torch's current one
     return dq, dk, dv
 
 
