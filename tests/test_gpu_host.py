@@ -165,3 +165,24 @@ def test_bwd_host_matches_device_backward(B, N, H, Hkv, d, causal):
     for g, r in zip((dq, dk, dv), refs):
         g = g.float().double().numpy()
         assert np.linalg.norm(g - r) / np.linalg.norm(r) <= 5e-3
+
+
+def test_binding_allocated_workspace_survives_reuse_pressure():
+    """A workspace the binding allocates is released while the library's
+    streams still use it; it is recorded on the caller's stream, so fresh
+    allocations (filled right away) cannot take its memory early."""
+    dev = torch.device("cuda:0")
+    s = torch.cuda.Stream(device=dev)
+    B, N, H, d = 3, 1024, 8, 128
+    q, k, v = host_qkv(B, N, H, H, d, seed=600)
+    with torch.cuda.stream(s):
+        o, lse = api.attn_fwd_host(q, k, v, causal=True, stream=s)
+        junk = [torch.full((1 << 22,), 7.0, device=dev) for _ in range(16)]   # 256 MB of new allocations
+    o2, lse2 = api.attn_fwd_host(q, k, v, causal=True, stream=s.cuda_stream)  # stream as a raw handle
+    torch.cuda.synchronize()
+    o_ref, lse_ref = api.attn_fwd(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    torch.cuda.synchronize()
+    for a, b_ in ((o, o_ref), (o2, o_ref)):
+        assert torch.equal(a.view(torch.int16), b_.cpu().view(torch.int16))
+    assert torch.equal(lse, lse_ref.cpu()) and torch.equal(lse2, lse_ref.cpu())
+    del junk
