@@ -24,8 +24,11 @@ PREP_SITES = {0x91}
 KNOWN_SITES = FWD_SITES
 
 
-def test_wait_timeout_is_reported_and_the_context_survives():
-    B, N, H, d = 1, 1024, 2, 128
+@pytest.mark.parametrize("d", [128, 256])
+def test_wait_timeout_is_reported_and_the_context_survives(d):
+    """d = 128 runs the two-tile kernel, d = 256 the one-tile kernel with
+    the S pipeline in tensor memory."""
+    B, N, H = 1, 1024, 2
     q, k, v = synth.qkv_bf16(B, N, H, d, seed=8)
     qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
     lib = api.library()
@@ -94,3 +97,19 @@ def test_prep_wait_timeout_is_reported_and_the_context_survives():
     got = api.attn_fp8_prep(xd, mode=api.MODE_BLOCK_HADAMARD, sign_seed=7)
     torch.cuda.synchronize()
     assert torch.equal(got[0], want[0]) and torch.equal(got[1], want[1])
+
+
+def test_fp8_head_dim_256_wait_timeout_is_reported_and_the_context_survives():
+    B, N, H, d = 1, 1024, 2, 256
+    q, k, v = synth.qkv_bf16(B, N, H, d, seed=10)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    q8, k8, v8, qs, ks, vs = api.fp8_prepare_qkv(qd, kd, vd, api.MODE_BLOCK_HADAMARD, 3)
+    want, want_lse = api.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True)
+    torch.cuda.synchronize()
+    rc, site = _timeout_then_recover(lambda: api.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True))
+    assert rc == ATTN_ERR_DEVICE_TIMEOUT, (rc, site)
+    assert site in FWD_SITES, hex(site)
+    got, got_lse = api.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16)) and torch.equal(got_lse, want_lse)
+    assert api.device_status()[0] == 0
