@@ -189,3 +189,26 @@ def test_bwd_host_workspace_and_arguments(lib):
     args = lambda d=128, wsb=ws: (FAKE,) * 9 + (B, H, Hkv, N, d, 1, 0.0, 0, FAKE, wsb, None)
     assert f(*args(d=256)) == -2
     assert f(*args(wsb=ws - 1)) == -1
+
+
+def test_host_bindings_check_their_arguments(lib):
+    """The host-buffer bindings reject device tensors, wrong dtypes, shapes
+    and outputs before calling the library (no GPU needed)."""
+    import torch
+    q = torch.zeros(2, 16, 4, 64, dtype=torch.bfloat16)
+    k = torch.zeros(2, 16, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        api.attn_fwd_host(q.float(), k, k)                      # dtype
+    with pytest.raises(ValueError):
+        api.attn_fwd_host(q, k, k[:, :8])                       # k / v shapes differ
+    with pytest.raises(ValueError):
+        api.attn_fwd_host(q, torch.zeros(2, 16, 3, 64, dtype=torch.bfloat16),
+                          torch.zeros(2, 16, 3, 64, dtype=torch.bfloat16))   # 3 does not divide 4
+    with pytest.raises(ValueError):
+        api.attn_fwd_host(q, k, k, out=torch.zeros(2, 16, 4, 32, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        api.attn_fwd_fp8_host(q, k, k, lse=torch.zeros(2, 4, 8))
+    with pytest.raises(ValueError):
+        api.attn_bwd_host(q[:, :8], q, k, k, q, torch.zeros(2, 4, 16))     # dout shaped unlike q
+    with pytest.raises(ValueError):
+        api.attn_bwd_host(q, q, k, k, q, torch.zeros(2, 4, 16), dk=torch.zeros(2, 16, 4, 64, dtype=torch.bfloat16))
