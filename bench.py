@@ -647,8 +647,19 @@ def main():
         line["roofline"]["note"] = ("achieved counts the whole backward step: the fused kernel plus the two "
                                     "memory-bound launches around it (D / accumulator zeroing, dQ conversion)")
 
+    if not args.quick:
+        # Every rank runs the end-to-end leg on its own shard at the same
+        # time (a barrier right before the timed loop); the job's figure is
+        # all ranks' work over the slowest rank's time.
+        e2e = e2e_measure(api, w, device, stream, arrs0, flops, steps=min(args.steps, 100),
+                          sync=(lambda: dist.barrier()) if ws > 1 else None)
+        if ws > 1:
+            t_e2e = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=device)
+            dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+            e2e = job_e2e(e2e, float(t_e2e.item()), ws, flops)
+        if rank == 0:
+            line["e2e"] = e2e
     if not args.quick and rank == 0:
-        line["e2e"] = e2e_measure(api, w, device, stream, arrs0, flops, steps=min(args.steps, 100))
         if w["dtype"] == "bf16" and args.workload == "c2":
             line["fp8"] = fp8_secondary(api, device, stream, steps=min(args.steps, 200))
             line["bwd"] = bwd_secondary(api, device, stream, steps=min(args.steps, 50))
@@ -659,13 +670,26 @@ def main():
         dist.destroy_process_group()
 
 
-def e2e_measure(api, w, device, stream, arrs, flops, steps):
+def job_e2e(rank_e2e: dict, ms_slowest: float, ws: int, flops_per_rank: float) -> dict:
+    """The whole job's end-to-end figure from one rank's: every rank moved
+    the same bytes and did the same work in its step, and the job's step
+    takes the slowest rank's time."""
+    out = dict(rank_e2e)
+    out["ms_per_step"] = round(ms_slowest, 4)
+    out["value"] = round(ws * flops_per_rank / (ms_slowest / 1e3) / 1e12, 2)
+    out["h2d_bytes_per_step"] = rank_e2e["h2d_bytes_per_step"] * ws
+    out["d2h_bytes_per_step"] = rank_e2e["d2h_bytes_per_step"] * ws
+    out["ranks"] = ws
+    return out
+
+
+def e2e_measure(api, w, device, stream, arrs, flops, steps, sync=None):
     """Same metric through the public API with HOST buffers: pinned host
     Q, K, V copied to the device, the forward, O and LSE copied back, all
     inside the timed region."""
     import torch
     if w.get("direction") == "bwd":
-        return e2e_measure_bwd(api, w, device, stream, arrs, flops, steps)
+        return e2e_measure_bwd(api, w, device, stream, arrs, flops, steps, sync)
     hmask = torch.from_numpy(block_mask(w)).pin_memory() if w.get("sparse") else None
     dmask = torch.empty_like(hmask, device=device) if hmask is not None else None
     hq, hk, hv = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for a in arrs)
@@ -728,6 +752,8 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps):
     for _ in range(3):
         step()
     torch.cuda.synchronize(device)
+    if sync:
+        sync()
     if host_path:
         ms = time_loop_two_streams(step, steps, streams) / steps
     else:
@@ -769,7 +795,7 @@ def bwd_secondary(api, device, stream, steps):
             "flop_convention": "2.5 x the forward's 4 B H N^2 d (five products against two)"}
 
 
-def e2e_measure_bwd(api, w, device, stream, arrs, flops, steps):
+def e2e_measure_bwd(api, w, device, stream, arrs, flops, steps, sync=None):
     """Backward end to end with HOST buffers: pinned Q, K, V, dO and the
     forward's O, LSE copied in, the backward, dQ, dK, dV copied back, all
     inside the timed region (through attn_bwd_host)."""
@@ -799,6 +825,8 @@ def e2e_measure_bwd(api, w, device, stream, arrs, flops, steps):
     for _ in range(3):
         step()
     torch.cuda.synchronize(device)
+    if sync:
+        sync()
     ms = time_loop_two_streams(step, steps, streams) / steps
     hgq, hgk, hgv = outs[0]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, ho, hl))

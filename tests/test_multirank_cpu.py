@@ -61,3 +61,16 @@ def test_two_gloo_ranks_shard_and_reduce(tmp_path):
     out = str(tmp_path / "result.txt")
     mp.start_processes(_rank_main, args=(2, _free_port(), out), nprocs=2, start_method="spawn", join=True)
     assert open(out).read() == "ok"
+
+
+def test_job_end_to_end_figure_from_the_slowest_rank():
+    """bench.py's end-to-end line at N ranks: all ranks' work over the
+    slowest rank's step time, bytes summed over the ranks."""
+    import bench
+    rank_e2e = {"value": 100.0, "unit": "TFLOPS", "h2d_bytes_per_step": 1000, "d2h_bytes_per_step": 10,
+                "ms_per_step": 1.0}
+    out = bench.job_e2e(rank_e2e, 2.0, 4, 1e12)
+    assert out["value"] == 2000.0          # 4 x 1e12 FLOP / 2 ms
+    assert out["h2d_bytes_per_step"] == 4000 and out["d2h_bytes_per_step"] == 40
+    assert out["ms_per_step"] == 2.0 and out["ranks"] == 4
+    assert rank_e2e["h2d_bytes_per_step"] == 1000   # the rank's own figure is left as it was
