@@ -8,11 +8,14 @@ block scales + Hadamard rotation, then the FP8 forward) is measured on its
 own workload (B=2, H=16, N=8192, d=128, non-causal, outlier inputs) and
 reported in the "fp8" object of the same line, and the backward on the
 pages' Fig. 6 point (B=1, H=16, N=16384, d=128, non-causal; FLOPs 2.5 x the
-forward's) in its "bwd" object.
+forward's) in its "bwd" object.  The "e2e" object is the same metric with
+host buffers, through the library's host-buffer entries (attn_fwd_host,
+attn_fwd_fp8_host, attn_bwd_host): the copies in and out are inside the
+timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c2|c4|c5|gqa|bwd|bwd_c2|bwd_d64|sparse|fp8_d256|c3:N:d:causal|fp8:N:d:causal|
-                                bwd:N:causal[:d]]
+                    [--workload c2|c4|c5|gqa|bwd|bwd_c2|bwd_d64|sparse|fp8_d256|fp8_d256_causal|
+                                c3:N:d:causal|fp8:N:d:causal|bwd:N:causal[:d]]
                     [--quick]
 
 Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
