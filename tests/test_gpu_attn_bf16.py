@@ -44,10 +44,26 @@ def test_short_and_boundary_lengths(N):
         assert_bf16_parity(e, f"N={N} causal={causal}")
 
 
+@pytest.mark.parametrize("N", [1, 5, 63, 64, 65, 127, 128, 129, 200])
+def test_short_and_boundary_lengths_head_dim_256(N):
+    """d = 256 runs the one-tile kernel with 64-key tiles and an S pipeline:
+    items of a single key tile (the ring then carries a stage with neither K
+    nor V), tails shorter than a tile and a pipeline shorter than its depth."""
+    for causal in (False, True):
+        e = run_case(2, N, 3, 256, causal=causal, seed=N + 1)
+        assert_bf16_parity(e, f"d=256 N={N} causal={causal}")
+
+
 @pytest.mark.parametrize("window", [1, 127, 128, 129, 300, 5000])
 def test_sliding_window(window):
     e = run_case(1, 1500, 2, 128, causal=True, window=window, seed=3)
     assert_bf16_parity(e, f"window={window}")
+
+
+@pytest.mark.parametrize("window", [1, 63, 64, 65, 300])
+def test_sliding_window_head_dim_256(window):
+    e = run_case(1, 900, 2, 256, causal=True, window=window, seed=6)
+    assert_bf16_parity(e, f"d=256 window={window}")
 
 
 def test_window_without_causal():
@@ -129,9 +145,12 @@ def _growing_scores(N, H, d, seed):
     return tuple(synth.to_bf16_bits(x) for x in (q, k, v))
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_growing_scores_exercise_rescaling(causal):
-    N, H, d = 1100, 2, 128
+def test_growing_scores_exercise_rescaling(causal, d):
+    """Scores that grow along the keys move the reference maximum often: the
+    O rescale (at d = 256 after waiting for the previous P V) is exercised."""
+    N, H = 1100, 2
     q, k, v = _growing_scores(N, H, d, seed=3)
     o, lse = api.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=causal)
     torch.cuda.synchronize()
