@@ -1,21 +1,23 @@
 """Benchmark of the fused exact-attention forward on GB300.
 
-Default workload: bf16 forward, B=2, H=32, N=4096, d=128, causal (the
-headline configuration), FLOPs counted as 4 B H N^2 d / 2.  One step = one
+Default workload: bf16 forward, B=1, H=16, N=16384, d=128, causal -- the
+d=128, N=16k point of the 16384-token sweep (hidden 2048), the largest bf16
+single-GPU configuration at the head dimension and length where the
+throughput target is set -- FLOPs counted as 4 B H N^2 d / 2.  One step = one
 fused forward over the batch (load, QK^T, online softmax, correction, PV and
-epilogue all inside one kernel launch).  The FP8 path (prep of Q, K, V with
-block scales + Hadamard rotation, then the FP8 forward) is measured on its
-own workload (B=2, H=16, N=8192, d=128, non-causal, outlier inputs) and
-reported in the "fp8" object of the same line, and the backward on the
-pages' Fig. 6 point (B=1, H=16, N=16384, d=128, non-causal; FLOPs 2.5 x the
-forward's) in its "bwd" object.  The "e2e" object is the same metric with
-host buffers, through the library's host-buffer entries (attn_fwd_host,
-attn_fwd_fp8_host, attn_bwd_host): the copies in and out are inside the
-timed region.
+epilogue all inside one kernel launch).  The same line carries, as extra
+objects: the non-causal variant of that point ("noncausal"), the B=2, H=32,
+N=4096 causal shape ("c2"), the FP8 path (prep of Q, K, V with block scales +
+Hadamard rotation, then the FP8 forward) on its workload (B=2, H=16, N=8192,
+d=128, non-causal, outlier inputs; "fp8"), and the backward on the pages'
+Fig. 6 point (B=1, H=16, N=16384, d=128, non-causal; FLOPs 2.5 x the
+forward's; "bwd").  The "e2e" object is the same metric with host buffers,
+through the library's host-buffer entries (attn_fwd_host, attn_fwd_fp8_host,
+attn_bwd_host): the copies in and out are inside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload c2|c4|c5|gqa|bwd|bwd_c2|bwd_d64|sparse|fp8_d256|fp8_d256_causal|
-                                c3:N:d:causal|fp8:N:d:causal|bwd:N:causal[:d]]
+                    [--workload c3_d128_n16k|c2|c4|c5|gqa|bwd|bwd_c2|bwd_d64|sparse|fp8_d256|
+                                fp8_d256_causal|c3:N:d:causal|fp8:N:d:causal|bwd:N:causal[:d]]
                     [--quick]
 
 Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
@@ -43,7 +45,13 @@ import numpy as np  # noqa: E402
 METRIC = "attention fwd TFLOPS (bf16, fp8) on 1 GB300 and % of dense tensor peak"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
+DEFAULT_WORKLOAD = "c3_d128_n16k"
+
 WORKLOADS = {
+    "c3_d128_n16k": dict(name="bf16 fwd B=1 H=16 N=16384 d=128 causal (16384 tokens, hidden 2048)", B=1, H=16,
+                         N=16384, d=128, causal=True, window=0, dtype="bf16"),
+    "c3_d128_n16k_noncausal": dict(name="bf16 fwd B=1 H=16 N=16384 d=128 non-causal (16384 tokens, hidden 2048)",
+                                   B=1, H=16, N=16384, d=128, causal=False, window=0, dtype="bf16"),
     "c2": dict(name="bf16 fwd B=2 H=32 N=4096 d=128 causal", B=2, H=32, N=4096, d=128, causal=True, window=0,
                dtype="bf16"),
     "c4": dict(name="fp8 e4m3 fwd B=2 H=16 N=8192 d=128 non-causal, outliers, block scales + Hadamard",
@@ -426,12 +434,12 @@ def run_reference(args, w, key):
 
 def measure_spec_peak():
     """Spec dense tensor peak pinned by this repository's own tcgen05
-    microbenchmark (csrc/peak/mma_peak.cu): SMs x measured dense FLOP per
+    microbenchmark (mma_peak.cu beside this file): SMs x measured dense FLOP per
     clock per SM x the maximum SM clock."""
-    src = os.path.join(ROOT, "exact_attention_71_gb300", "csrc", "peak", "mma_peak.cu")
+    src = os.path.join(ROOT, "mma_peak.cu")
     exe = os.path.join(ROOT, "_build", "mma_peak")
     os.makedirs(os.path.dirname(exe), exist_ok=True)
-    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-o", exe, src],
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-I", ROOT, "-o", exe, src],
                    check=True)
     res = json.loads(subprocess.run([exe], check=True, capture_output=True, text=True).stdout.strip())
     mhz = res["max_sm_mhz"]
@@ -504,7 +512,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--quick", action="store_true", help="skip e2e, FP8 and CPU baseline (profiling runs)")
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--fp8-peak", action="store_true", help="measure the cuBLASLt e4m3 GEMM peak and exit")
@@ -663,7 +671,10 @@ def main():
         if rank == 0:
             line["e2e"] = e2e
     if not args.quick and rank == 0:
-        if w["dtype"] == "bf16" and args.workload == "c2":
+        if args.workload == DEFAULT_WORKLOAD:
+            line["noncausal"] = fwd_secondary(api, device, stream, "c3_d128_n16k_noncausal",
+                                              steps=min(args.steps, 200))
+            line["c2"] = fwd_secondary(api, device, stream, "c2", steps=min(args.steps, 200))
             line["fp8"] = fp8_secondary(api, device, stream, steps=min(args.steps, 200))
             line["bwd"] = bwd_secondary(api, device, stream, steps=min(args.steps, 50))
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.ref_budget, arrs=arrs0)
@@ -769,6 +780,34 @@ def e2e_measure(api, w, device, stream, arrs, flops, steps, sync=None):
         out["api"] = (("attn_fwd_fp8_host" if fp8 else "attn_fwd_host") +
                       " (pinned host buffers; per-sequence chunks, copies overlapped with the compute; two streams)")
     return out
+
+
+def fwd_secondary(api, device, stream, key, steps):
+    """A further bf16 forward workload, timed like the main line (two
+    resident input sets larger than L2, alternated per step)."""
+    import torch
+    w = dict(WORKLOADS[key])
+    sets = [make_inputs(w, device, seed=s)[0] for s in range(2)]
+    B, H, N, d = w["B"], w["H"], w["N"], w["d"]
+    o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    idx = [0]
+
+    def fn():
+        q, k, v = sets[idx[0] & 1]
+        idx[0] += 1
+        api.attn_fwd(q, k, v, causal=w["causal"], window=w["window"], out=o, lse=lse, stream=stream)
+
+    for _ in range(5):
+        fn()
+    torch.cuda.synchronize(device)
+    ms = time_loop(fn, steps, stream) / steps
+    flops = flops_per_step(w)
+    peaks, src = load_peaks()
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": w["name"], "flops_per_step": flops, "ms": round(ms, 5), "tflops": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "steps": steps,
+            "traffic": recorded_traffic("attn_fwd", key)}
 
 
 def bwd_secondary(api, device, stream, steps):

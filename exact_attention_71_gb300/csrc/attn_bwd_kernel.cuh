@@ -1,4 +1,4 @@
-// Fused exact-attention backward for sm_103a (bf16, head_dim 128).
+// Fused exact-attention backward for sm_103a (bf16, head_dim 64 and 128).
 //
 // Method (FlashAttention-3 deep-reading report §3.4: the backward keeps
 // FA2's recompute strategy, five matrix products against the forward's

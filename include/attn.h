@@ -33,8 +33,10 @@
  *    default stream).  Argument errors are detected before any launch.
  *  - Return value: ATTN_OK or a negative attn_status.  The text of the last
  *    error of the calling thread is available from attn_last_error_string().
- *  - Rows that can see no key (only possible with a window and no causal
- *    mask at the sequence end) get O = 0 and LSE = -inf.
+ *  - Under the causal and window masks alone every query sees at least
+ *    itself.  Only attn_fwd_sparse can leave a row with no visible key (its
+ *    block mask hides every key block of the row's query tile); such rows
+ *    get O = 0 and LSE = -inf.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H

@@ -5,8 +5,9 @@
 // FLOP per clock per SM = 2 * 128 * 256 * K * count / cycles.  bf16
 // (kind::f16, K = 16) and e4m3 (kind::f8f6f4, K = 32).
 //
-// Standalone program (not part of the attention library):
-//   nvcc -gencode arch=compute_103a,code=sm_103a -O3 -std=c++17 -o mma_peak mma_peak.cu
+// Standalone measurement program, built and run by `bench.py --spec-peak`
+// (not part of the attention library):
+//   nvcc -gencode arch=compute_103a,code=sm_103a -O3 -std=c++17 -I. -o mma_peak mma_peak.cu   (from the repository root)
 //   ./mma_peak      -> one JSON line
 #include <cuda_runtime.h>
 
@@ -14,7 +15,7 @@
 #include <cstdlib>
 #include <vector>
 
-#include "../sm103_ptx.cuh"
+#include "exact_attention_71_gb300/csrc/sm103_ptx.cuh"
 
 using namespace attn;
 

@@ -1,5 +1,7 @@
 """bf16 fused forward vs the fp64 oracle on the same seeded inputs, through
 the C ABI (max-abs <= 1e-2, RMS <= 2e-3, LSE <= 1e-3)."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -120,14 +122,29 @@ def test_repeat_is_bitwise_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("N", [512, 2048, 16384])
-@pytest.mark.parametrize("d", [64, 128, 256])
+@functools.lru_cache(maxsize=1)
+def _sweep_inputs(N, d):
+    """The sweep point's Q, K, V (the causal and non-causal cases share them)."""
+    return synth.qkv_bf16(16384 // N, N, 2048 // d, d, seed=11)
+
+
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("N", [512, 1024, 2048, 4096, 8192, 16384])
 def test_config3_sweep_sampled_rows(N, d, causal):
-    """16384 tokens, hidden 2048: B = 16384 / N, H = 2048 / d."""
+    """16384 tokens, hidden 2048: B = 16384 / N, H = 2048 / d; every point of
+    the sweep, 256 sampled query rows of every head (first and last rows,
+    tile-boundary rows, the rows around each 1024-row boundary and seeded
+    picks)."""
     B, H = 16384 // N, 2048 // d
-    rows = synth.sample_rows(N, 24, seed=N + d)
-    e = run_case(B, N, H, d, causal=causal, rows=rows, seed=11)
+    q, k, v = _sweep_inputs(N, d)
+    must = [r for x in range(1024, N, 1024) for r in (x - 1, x)]
+    rows = synth.sample_rows(N, 256, seed=N + d, must=must)
+    o, lse = api.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=causal)
+    torch.cuda.synchronize()
+    assert api.device_status()[0] == 0
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=causal, rows=rows)
+    e = errors(gpu_rows(o, rows), o_ref, lse_rows(lse, rows), lse_ref)
     assert_bf16_parity(e, f"C3 N={N} d={d} causal={causal}")
 
 
