@@ -186,6 +186,40 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity, const
     return true;
 }
 
+// FP8: the largest V block scale of one (batch, key/value head), the
+// normaliser of the V factors folded into P (P8 = e4m3(P * P8_SCALE *
+// v_scale_j / vmax)).  Every lane of the warp loads every 32nd block scale
+// and the warp reduces them, so each warp gets the same value without any
+// cross-warp synchronisation.  1 when every scale is 0.
+__device__ __forceinline__ float fp8_vmax(const float* vs, int nblk) {
+    float v = 0.0f;
+    for (int x = static_cast<int>(lane_id()); x < nblk; x += 32) v = fmaxf(v, __ldg(vs + x));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v > 0.0f ? v : 1.0f;
+}
+
+// FP8: the factors of one key tile's softmax step, from the K and V block
+// scales of the 128-key block `sb`: mult takes the raw e4m3 scores to log2
+// units (softmax scale * log2 e * q_scale * k_scale), lg = log2(pv_mult) is
+// added to the exponent so that exp2 yields P * pv_mult directly (the V
+// block's factor folded into P), and inv = 1 / pv_mult turns the tile's sum
+// back into a sum of P.  The softmax loads these one step ahead, while it
+// waits for the next S, so that no global load, division or logarithm lies
+// between an S becoming visible and its P being handed over.
+template <class Cfg>
+__device__ __forceinline__ void fp8_tile_scales(const FwdParams& p, size_t sb, float q_mult, float vmax, float& mult,
+                                                float& lg, float& inv) {
+    mult = q_mult * __ldg(p.k_scale + sb);
+    const float pv_mult = Cfg::P8_SCALE * (__ldg(p.v_scale + sb) / vmax);
+    lg = __log2f(pv_mult);
+    inv = 1.0f / pv_mult;
+}
+
+// Makes three values available at this point of the program (the compiler
+// may not sink their computation below it, e.g. past a barrier wait).
+__device__ __forceinline__ void pin3(float& a, float& b, float& c) { asm volatile("" : "+f"(a), "+f"(b), "+f"(c)); }
+
 template <class Cfg>
 __device__ __forceinline__ void tile_range(const FwdParams& p, int qs, int& lo, int& hi) {
     const int qe = min(qs + Cfg::BM, p.N) - 1;
@@ -677,13 +711,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             float q_mult = p.scale_log2;
             // Key/value head of this query head (grouped-query attention).
             const int bh_kv = b * (p.H / p.group) + h / p.group;
+            const size_t sb0 = static_cast<size_t>(bh_kv) * nblk;
             if constexpr (Cfg::FP8) {
-                const float* vs = p.v_scale + static_cast<size_t>(bh_kv) * nblk;
-                vmax = 0.0f;
-                for (int x = 0; x < nblk; ++x) vmax = fmaxf(vmax, vs[x]);
-                if (!(vmax > 0.0f)) vmax = 1.0f;
-                q_mult *= p.q_scale[static_cast<size_t>(bh) * nblk + qs / 128];
+                vmax = fp8_vmax(p.v_scale + sb0, nblk);
+                q_mult *= __ldg(p.q_scale + static_cast<size_t>(bh) * nblk + qs / 128);
             }
+            // FP8 factors of the next key tile (bf16: the scale alone).
+            float nx_mult = q_mult, nx_lg = 0.0f, nx_inv = 1.0f;
+            if constexpr (Cfg::FP8)
+                fp8_tile_scales<Cfg>(p, sb0 + (tk.first * BN) / 128, q_mult, vmax, nx_mult, nx_lg, nx_inv);
             float m = -INFINITY;   // reference maximum of the log2-scaled scores
             float l = 0.0f;        // running sum of exp2(score - m)
             bool first_tile = true;
@@ -694,13 +730,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                float mult = q_mult;
-                float pv_mult = 1.0f;
-                if constexpr (Cfg::FP8) {
-                    const size_t sb = static_cast<size_t>(bh_kv) * nblk + (j * BN) / 128;
-                    mult *= p.k_scale[sb];
-                    pv_mult = Cfg::P8_SCALE * (p.v_scale[sb] / vmax);
-                }
+                const float mult = nx_mult;
                 uint32_t sr[BN];
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_tmem + c * 32, sr + c * 32);
@@ -764,7 +794,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 } else {
                     // P * pv_mult = exp2(x + log2(pv_mult)): the V block scale
                     // rides in the exponent; the tile's sum is divided by it once.
-                    const float lg = __log2f(pv_mult);
+                    const float lg = nx_lg;
                     const float2 negs = make_float2(-m_use + lg, -m_use + lg);
 #pragma unroll
                     for (int c = 0; c < BN / 64; ++c) {
@@ -786,7 +816,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         }
                         tmem_st16(s_tmem + c * 16, pk);
                     }
-                    const float inv = 1.0f / pv_mult;
+                    const float inv = nx_inv;
                     acc0.x *= inv; acc0.y *= inv; acc1.x *= inv; acc1.y *= inv;
                 }
                 const float rsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
@@ -809,6 +839,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&bars->p_full[t]);
+                if constexpr (Cfg::FP8) {
+                    const int jn = next_in<Cfg>(tk, j);
+                    if (jn >= 0) {
+                        fp8_tile_scales<Cfg>(p, sb0 + (jn * BN) / 128, q_mult, vmax, nx_mult, nx_lg, nx_inv);
+                        pin3(nx_mult, nx_lg, nx_inv);
+                    }
+                }
                 m = m_new;
                 first_tile = false;
                 ++count;

@@ -289,13 +289,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             float vmax = 1.0f;
             float q_mult = p.scale_log2;
             const int bh_kv = b * (p.H / p.group) + h / p.group;
+            const size_t sb0 = static_cast<size_t>(bh_kv) * nblk;
             if constexpr (Cfg::FP8) {
-                const float* vs = p.v_scale + static_cast<size_t>(bh_kv) * nblk;
-                vmax = 0.0f;
-                for (int x = 0; x < nblk; ++x) vmax = fmaxf(vmax, vs[x]);
-                if (!(vmax > 0.0f)) vmax = 1.0f;
-                q_mult *= p.q_scale[static_cast<size_t>(bh) * nblk + qs / 128];
+                vmax = fp8_vmax(p.v_scale + sb0, nblk);
+                q_mult *= __ldg(p.q_scale + static_cast<size_t>(bh) * nblk + qs / 128);
             }
+            // FP8 factors of the next key tile, loaded one step ahead (bf16:
+            // the scale alone).
+            float nx_mult = q_mult, nx_lg = 0.0f, nx_inv = 1.0f;
+            if constexpr (Cfg::FP8)
+                fp8_tile_scales<Cfg>(p, sb0 + (tk.first * BN) / 128, q_mult, vmax, nx_mult, nx_lg, nx_inv);
             float m = -INFINITY;
             float l = 0.0f;
             bool first_tile = true;
@@ -313,13 +316,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) reg_fence32(sr + c * 32);
-                float mult = q_mult;
-                float pv_mult = 1.0f;
-                if constexpr (Cfg::FP8) {
-                    const size_t sbk = static_cast<size_t>(bh_kv) * nblk + (j * BN) / 128;
-                    mult *= p.k_scale[sbk];
-                    pv_mult = Cfg::P8_SCALE * (p.v_scale[sbk] / vmax);
-                }
+                const float mult = nx_mult;
                 const int kbase = j * BN;
                 if (kbase < klo || kbase + BN - 1 > khi) {
 #pragma unroll
@@ -369,7 +366,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 } else {
                     // P * pv_mult = exp2(x + log2(pv_mult)): the V block scale
                     // rides in the exponent; the tile's sum is divided by it once.
-                    const float lg = __log2f(pv_mult);
+                    const float lg = nx_lg;
                     const float2 negs = make_float2(-m_use + lg, -m_use + lg);
 #pragma unroll
                     for (int c = 0; c < BN / 64; ++c) {
@@ -391,7 +388,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         }
                         tmem_st16(p_tm + c * 16, pk);
                     }
-                    const float inv = 1.0f / pv_mult;
+                    const float inv = nx_inv;
                     acc0.x *= inv; acc0.y *= inv; acc1.x *= inv; acc1.y *= inv;
                 }
                 const float rsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
@@ -420,6 +417,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->p_full[sb]);
+                if constexpr (Cfg::FP8) {
+                    const int jn = next_in<Cfg>(tk, j);
+                    if (jn >= 0) {
+                        fp8_tile_scales<Cfg>(p, sb0 + (jn * BN) / 128, q_mult, vmax, nx_mult, nx_lg, nx_inv);
+                        pin3(nx_mult, nx_lg, nx_inv);
+                    }
+                }
                 m = m_new;
                 first_tile = false;
                 ++s_cnt;
