@@ -107,9 +107,9 @@ struct FwdCfg {
     static constexpr int BAR_BYTES = 256;
     // The reference maximum of a row moves only when the row maximum exceeds
     // it by more than this (log2 units), so P <= 2^RESCALE_LOG2.  FP8 scales P
-    // by P8_SCALE = 2^(8 - RESCALE_LOG2) before the e4m3 cast (P * P8_SCALE
-    // <= 256 < 448, the largest e4m3 value).
-    static constexpr float RESCALE_LOG2 = FP8 ? 4.0f : 8.0f;
+    // by P8_SCALE = 16 before the e4m3 cast: P * P8_SCALE <= 2^4.8 * 16 ~ 445.7
+    // < 448, the largest e4m3 value (and the V factor folded in is <= 1).
+    static constexpr float RESCALE_LOG2 = FP8 ? 4.8f : 8.0f;
     static constexpr float P8_SCALE = FP8 ? 16.0f : 1.0f;
     // Register split: the launch gives every thread LAUNCH_REGS; the load /
     // MMA warpgroup drops to LOW_REGS and the softmax warpgroups rise to
@@ -824,17 +824,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // Rescale the accumulator of the rows whose maximum moved.  The
                 // commit that signalled S_t(j) also covers O_t += P_t V_{j-1}, so
                 // O_t is stable here; the next P V waits for p_full below.
+                // The whole row is loaded before one wait (one TMEM round trip
+                // instead of one per 32 columns); S is dead by now.
                 if (!first_tile && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                    uint32_t orr[D];
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t orr[32];
-                        tmem_ld32(o_tmem + c * 32, orr);
-                        tmem_wait_ld();
-                        reg_fence32(orr);
+                    for (int c = 0; c < D / 32; ++c) tmem_ld32(o_tmem + c * 32, orr + c * 32);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int x = 0; x < 32; ++x) orr[x] = __float_as_uint(__uint_as_float(orr[x]) * alpha);
-                        tmem_st32(o_tmem + c * 32, orr);
+                    for (int c = 0; c < D / 32; ++c) reg_fence32(orr + c * 32);
+                    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+                    for (int x = 0; x < D; x += 2) {
+                        const float2 v =
+                            __fmul2_rn(make_float2(__uint_as_float(orr[x]), __uint_as_float(orr[x + 1])), a2);
+                        orr[x] = __float_as_uint(v.x);
+                        orr[x + 1] = __float_as_uint(v.y);
                     }
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) tmem_st32(o_tmem + c * 32, orr + c * 32);
                 }
                 tmem_wait_st();
                 tc_fence_before();

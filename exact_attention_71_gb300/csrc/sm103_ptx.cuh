@@ -310,12 +310,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Four floats -> packed e4m3x4 (x0 in bits 0-7), round to nearest even,
-// saturating to the largest finite value.
+// saturating to the largest finite value.  One asm block, so that the two
+// 16-bit halves are joined by a single move.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
-    uint16_t lo, hi;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+    return r;
 }
 
 }  // namespace attn

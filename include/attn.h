@@ -85,9 +85,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * rotation leaves Q K^T unchanged.  V's block scale lies on the contraction
  * dimension of P V, so it is folded into P before P is rounded to e4m3:
  * P8 = e4m3(P * 16 * v_scale_j / vmax) with vmax the largest V block scale
- * of the (batch, head) and P <= 16 (the row maximum used in P moves only when
- * a score exceeds it by more than 4 in log2 units); O = (sum P8 V8) * vmax /
- * (16 * l).  d must be 64, 128 or 256 (ATTN_ERR_UNSUPPORTED otherwise).
+ * of the (batch, head) and P <= 2^4.8 (the row maximum used in P moves only
+ * when a score exceeds it by more than 4.8 in log2 units, so P * 16 <= 445.7
+ * stays below e4m3's largest value, 448); O = (sum P8 V8) * vmax / (16 * l).  d must be 64, 128 or 256 (ATTN_ERR_UNSUPPORTED otherwise).
  */
 int attn_fwd_fp8(const void* q8, const void* k8, const void* v8, void* o, float* lse,
                  int B, int H, int N, int d, int causal, float scale, int window,
