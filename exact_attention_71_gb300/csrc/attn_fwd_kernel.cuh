@@ -794,28 +794,39 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 } else {
                     // P * pv_mult = exp2(x + log2(pv_mult)): the V block scale
                     // rides in the exponent; the tile's sum is divided by it once.
+                    // The exponentials are taken two at a time in f16 (FP16
+                    // intermediates of the FP8 path, deep-reading report §3.3):
+                    // half the MUFU work, and P is rounded to e4m3 next anyway.
+                    // The row sum is kept in four f16x2 partial sums (P * pv_mult
+                    // <= 445.7, 16 terms per half: <= 7132 < 65504).
                     const float lg = nx_lg;
                     const float2 negs = make_float2(-m_use + lg, -m_use + lg);
+                    uint32_t hs0 = 0u, hs1 = 0u, hs2 = 0u, hs3 = 0u;
 #pragma unroll
                     for (int c = 0; c < BN / 64; ++c) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int x = 0; x < 16; ++x) {
                             const int e = c * 64 + 4 * x;
-                            float2 t0 = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                                   mult2, negs);
-                            float2 t1 = __ffma2_rn(
+                            const float2 t0 = __ffma2_rn(
+                                make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), mult2, negs);
+                            const float2 t1 = __ffma2_rn(
                                 make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), mult2, negs);
-                            t0.x = ex2_approx(t0.x);
-                            t0.y = ex2_approx(t0.y);
-                            t1.x = ex2_approx(t1.x);
-                            t1.y = ex2_approx(t1.y);
-                            acc0 = __fadd2_rn(acc0, t0);
-                            acc1 = __fadd2_rn(acc1, t1);
-                            pk[x] = pack_e4m3x4(t0.x, t0.y, t1.x, t1.y);
+                            const uint32_t p01 = ex2_f16x2(pack_f16x2(t0.x, t0.y));
+                            const uint32_t p23 = ex2_f16x2(pack_f16x2(t1.x, t1.y));
+                            if (x & 1) {
+                                hs2 = add_f16x2(hs2, p01);
+                                hs3 = add_f16x2(hs3, p23);
+                            } else {
+                                hs0 = add_f16x2(hs0, p01);
+                                hs1 = add_f16x2(hs1, p23);
+                            }
+                            pk[x] = pack_e4m3x4_f16(p01, p23);
                         }
                         tmem_st16(s_tmem + c * 16, pk);
                     }
+                    acc0 = __fadd2_rn(f16x2_to_float2(hs0), f16x2_to_float2(hs2));
+                    acc1 = __fadd2_rn(f16x2_to_float2(hs1), f16x2_to_float2(hs3));
                     const float inv = nx_inv;
                     acc0.x *= inv; acc0.y *= inv; acc1.x *= inv; acc1.y *= inv;
                 }

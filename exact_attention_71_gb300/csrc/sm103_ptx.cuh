@@ -309,6 +309,48 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// Two floats -> packed f16x2 (lo in bits 0-15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Hardware base-2 exponential of both halves of an f16x2 (MUFU, one
+// instruction for two values); ex2(-inf) = +0.
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+    uint32_t y;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t add_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t x) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(x));
+    return make_float2(lo, hi);
+}
+
+// Two f16x2 (values 0, 1 and 2, 3) -> packed e4m3x4 (value 0 in bits 0-7),
+// round to nearest even, saturating to the largest finite value.
+__device__ __forceinline__ uint32_t pack_e4m3x4_f16(uint32_t v01, uint32_t v23) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f16x2 lo, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f16x2 hi, %2;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "r"(v01), "r"(v23));
+    return r;
+}
+
 // Four floats -> packed e4m3x4 (x0 in bits 0-7), round to nearest even,
 // saturating to the largest finite value.  One asm block, so that the two
 // 16-bit halves are joined by a single move.

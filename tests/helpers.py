@@ -9,6 +9,15 @@ BF16_MAX_ABS = 1e-2
 BF16_RMS = 2e-3
 LSE_ABS = 1e-3
 FP8_RMS = 3e-2
+# FP8 path, LSE against the oracle run on the dequantised codes.  P's
+# exponentials use FP16 intermediates: the argument (which carries the V
+# block factor's log2, <= 4, so the keys that carry the weight have arguments
+# up to 8.8) is rounded to f16, at most 2^-8 absolute there, i.e. <= 2.7e-3
+# relative in P; the f16 result adds ~2^-10; the row sum is kept in f16
+# partial sums of 16 terms (~4 * 2^-11 / sqrt(3) ~ 1.1e-3 random-walk,
+# 16 * 2^-11 ~ 7.8e-3 worst case).  ln l is off by their sum, ~5e-3 in the
+# worst rows of a large sample; gated at 1e-2.
+FP8_LSE = 1e-2
 
 
 def to_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:

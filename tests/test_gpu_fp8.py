@@ -25,6 +25,15 @@ sum as attention with |V| in place of V -- plus the bf16 rounding of O and a
 worst-case; random rounding errors give a relative RMS error of about
 2^-4 / sqrt(3) / 1.44 ~ 2.5 %, gated at 5 %, which a dropped or repeated
 128-key tile (1/32 of the weight at N = 4096, ~18 % relative) exceeds.
+
+LSE bound of the same comparison (FP8_LSE in tests/helpers.py).  The FP8
+path takes P's exponentials with FP16 intermediates (the FP8 design of the
+deep-reading report, §3.3): the f16 argument, the f16 exponential and the f16
+partial row sums put l off by up to ~0.5 % in the worst sampled rows; the same
+P enter O's numerator and l, so O does not see it, but LSE = ln l does.  The
+O bound above is unchanged: P is rounded to e4m3 after the f16 exponential,
+and the 2^-4 of the e4m3 rounding dominates (the 2^-10 term covers the rest
+for these magnitudes).
 """
 import numpy as np
 import pytest
@@ -32,7 +41,7 @@ import torch
 
 import oracle
 from exact_attention_71_gb300 import api, synth
-from tests.helpers import FP8_RMS, bf16_half_ulp, gpu_rows, lse_rows, to_dev
+from tests.helpers import FP8_LSE, FP8_RMS, bf16_half_ulp, gpu_rows, lse_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -136,7 +145,7 @@ def _assert_dequant_parity(o, lse, prepped, rows, causal=False, window=0, label=
     print(f"{label}: max-abs {err.max():.3e} (worst err/bound {worst:.3f}) rel-RMS {rel_rms:.3e} LSE {lerr:.2e}")
     assert worst <= 1.0, (label, worst, float(err.max()))
     assert rel_rms <= FP8_REL_RMS, (label, rel_rms)
-    assert lerr <= 1e-3, (label, lerr)
+    assert lerr <= FP8_LSE, (label, lerr)
     assert api.device_status()[0] == 0
 
 
