@@ -111,6 +111,10 @@ struct FwdCfg {
     // < 448, the largest e4m3 value (and the V factor folded in is <= 1).
     static constexpr float RESCALE_LOG2 = FP8 ? 4.8f : 8.0f;
     static constexpr float P8_SCALE = FP8 ? 16.0f : 1.0f;
+    // FP8: when the reference moves, it is set this far (log2 units) above
+    // the new row maximum, so that the next moves need a larger jump (the
+    // outlier workload's maxima grow in jumps); the tile's P are then <= 1/4.
+    static constexpr float RESCALE_HEADROOM = FP8 ? 2.0f : 0.0f;
     // Register split: the launch gives every thread LAUNCH_REGS; the load /
     // MMA warpgroup drops to LOW_REGS and the softmax warpgroups rise to
     // HIGH_REGS.  The sum stays within the launch allocation.
@@ -203,17 +207,20 @@ __device__ __forceinline__ float fp8_vmax(const float* vs, int nblk) {
 // scales of the 128-key block `sb`: mult takes the raw e4m3 scores to log2
 // units (softmax scale * log2 e * q_scale * k_scale), lg = log2(pv_mult) is
 // added to the exponent so that exp2 yields P * pv_mult directly (the V
-// block's factor folded into P), and inv = 1 / pv_mult turns the tile's sum
-// back into a sum of P.  The softmax loads these one step ahead, while it
-// waits for the next S, so that no global load, division or logarithm lies
-// between an S becoming visible and its P being handed over.
+// block's factor, pv_mult = P8_SCALE * v_scale / vmax, folded into P), and
+// inv = 2^-lg turns the tile's sum back into a sum of P (the inverse of the
+// factor actually applied, so P's weights and l stay consistent).  inv_vmax
+// is 1 / vmax, taken once per item: no division per key tile.  The softmax
+// loads these one step ahead, while it waits for the next S, so that no
+// global load or logarithm lies between an S becoming visible and its P
+// being handed over.
 template <class Cfg>
-__device__ __forceinline__ void fp8_tile_scales(const FwdParams& p, size_t sb, float q_mult, float vmax, float& mult,
-                                                float& lg, float& inv) {
+__device__ __forceinline__ void fp8_tile_scales(const FwdParams& p, size_t sb, float q_mult, float inv_vmax,
+                                                float& mult, float& lg, float& inv) {
     mult = q_mult * __ldg(p.k_scale + sb);
-    const float pv_mult = Cfg::P8_SCALE * (__ldg(p.v_scale + sb) / vmax);
+    const float pv_mult = Cfg::P8_SCALE * (__ldg(p.v_scale + sb) * inv_vmax);
     lg = __log2f(pv_mult);
-    inv = 1.0f / pv_mult;
+    inv = ex2_approx(-lg);
 }
 
 // Makes three values available at this point of the program (the compiler
@@ -707,19 +714,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // Visible keys of row i: [klo, khi].
             const int klo = p.window > 0 ? i - p.window + 1 : 0;
             const int khi = p.causal ? min(i, p.N - 1) : p.N - 1;
-            float vmax = 1.0f;
+            float vmax = 1.0f, ivmax = 1.0f;
             float q_mult = p.scale_log2;
             // Key/value head of this query head (grouped-query attention).
             const int bh_kv = b * (p.H / p.group) + h / p.group;
             const size_t sb0 = static_cast<size_t>(bh_kv) * nblk;
             if constexpr (Cfg::FP8) {
                 vmax = fp8_vmax(p.v_scale + sb0, nblk);
+                ivmax = 1.0f / vmax;
                 q_mult *= __ldg(p.q_scale + static_cast<size_t>(bh) * nblk + qs / 128);
             }
             // FP8 factors of the next key tile (bf16: the scale alone).
             float nx_mult = q_mult, nx_lg = 0.0f, nx_inv = 1.0f;
             if constexpr (Cfg::FP8)
-                fp8_tile_scales<Cfg>(p, sb0 + (tk.first * BN) / 128, q_mult, vmax, nx_mult, nx_lg, nx_inv);
+                fp8_tile_scales<Cfg>(p, sb0 + (tk.first * BN) / 128, q_mult, ivmax, nx_mult, nx_lg, nx_inv);
             float m = -INFINITY;   // reference maximum of the log2-scaled scores
             float l = 0.0f;        // running sum of exp2(score - m)
             bool first_tile = true;
@@ -765,7 +773,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // exactly so that P <= 1 before the e4m3 scaling.
                 const float m_tile = mx * mult;
                 float m_new = m;
-                if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY) m_new = fmaxf(m, m_tile);
+                if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY)
+                    m_new = fmaxf(m, m_tile + Cfg::RESCALE_HEADROOM);
                 // A row that has seen no visible key yet keeps m = -inf (so
                 // that its first real scores set the reference, however
                 // negative); its exponent reference is then 0 and its P is 0.
@@ -861,7 +870,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if constexpr (Cfg::FP8) {
                     const int jn = next_in<Cfg>(tk, j);
                     if (jn >= 0) {
-                        fp8_tile_scales<Cfg>(p, sb0 + (jn * BN) / 128, q_mult, vmax, nx_mult, nx_lg, nx_inv);
+                        fp8_tile_scales<Cfg>(p, sb0 + (jn * BN) / 128, q_mult, ivmax, nx_mult, nx_lg, nx_inv);
                         pin3(nx_mult, nx_lg, nx_inv);
                     }
                 }

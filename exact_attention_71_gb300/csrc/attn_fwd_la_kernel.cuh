@@ -286,19 +286,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             const int klo = p.window > 0 ? i - p.window + 1 : 0;
             const int khi = p.causal ? min(i, p.N - 1) : p.N - 1;
-            float vmax = 1.0f;
+            float vmax = 1.0f, ivmax = 1.0f;
             float q_mult = p.scale_log2;
             const int bh_kv = b * (p.H / p.group) + h / p.group;
             const size_t sb0 = static_cast<size_t>(bh_kv) * nblk;
             if constexpr (Cfg::FP8) {
                 vmax = fp8_vmax(p.v_scale + sb0, nblk);
+                ivmax = 1.0f / vmax;
                 q_mult *= __ldg(p.q_scale + static_cast<size_t>(bh) * nblk + qs / 128);
             }
             // FP8 factors of the next key tile, loaded one step ahead (bf16:
             // the scale alone).
             float nx_mult = q_mult, nx_lg = 0.0f, nx_inv = 1.0f;
             if constexpr (Cfg::FP8)
-                fp8_tile_scales<Cfg>(p, sb0 + (tk.first * BN) / 128, q_mult, vmax, nx_mult, nx_lg, nx_inv);
+                fp8_tile_scales<Cfg>(p, sb0 + (tk.first * BN) / 128, q_mult, ivmax, nx_mult, nx_lg, nx_inv);
             float m = -INFINITY;
             float l = 0.0f;
             bool first_tile = true;
@@ -339,7 +340,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const float mx = fmax3(mx0, mx2, fmaxf(__uint_as_float(sr[BN - 2]), __uint_as_float(sr[BN - 1])));
                 const float m_tile = mx * mult;
                 float m_new = m;
-                if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY) m_new = fmaxf(m, m_tile);
+                if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY)
+                    m_new = fmaxf(m, m_tile + Cfg::RESCALE_HEADROOM);
                 const float m_use = m_new == -INFINITY ? 0.0f : m_new;
                 const float alpha = ex2_approx(m - m_use);
                 const float2 mult2 = make_float2(mult, mult);
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if constexpr (Cfg::FP8) {
                     const int jn = next_in<Cfg>(tk, j);
                     if (jn >= 0) {
-                        fp8_tile_scales<Cfg>(p, sb0 + (jn * BN) / 128, q_mult, vmax, nx_mult, nx_lg, nx_inv);
+                        fp8_tile_scales<Cfg>(p, sb0 + (jn * BN) / 128, q_mult, ivmax, nx_mult, nx_lg, nx_inv);
                         pin3(nx_mult, nx_lg, nx_inv);
                     }
                 }
