@@ -52,6 +52,8 @@ def library() -> ctypes.CDLL:
         L.attn_fwd_fp8_gqa.argtypes = [P, P, P, P, P, i, i, i, i, i, i, f, i, P, P, P, P]
         L.attn_fwd_fp8_gqa.restype = i
         L.attn_fp8_prep.argtypes = [P, P, P, i, i, i, i, i, i, u64, i, P]
+        L.attn_fp8_prep_qkv.argtypes = [P, P, P, P, P, P, P, P, P, i, i, i, i, i, i, u64, P]
+        L.attn_fp8_prep_qkv.restype = i
         L.attn_fp8_prep_rope.argtypes = [P, P, P, P, P, i, i, i, i, i, i, u64, i, P]
         L.attn_fp8_prep_rope.restype = i
         L.attn_fp8_prep.restype = i
@@ -443,13 +445,39 @@ def attn_fp8_prep_rope(x, rope_cos, rope_sin, mode: int = MODE_BLOCK_HADAMARD, s
     return out, scales
 
 
+def attn_fp8_prep_qkv(q, k, v, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0, stream=None):
+    """The prep of Q, K (rotated in mode 1) and V (never rotated) in one call
+    (one launch for modes 0 and 1 at head dims 64 and 128).
+
+    Returns (q8, k8, v8, q_scale, k_scale, v_scale)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 (B, N, H, d) CUDA tensor")
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be (B, N, H_kv, d) with q's B, N and d")
+    nblk = (N + BLOCK_ROWS - 1) // BLOCK_ROWS
+    q8 = torch.empty((B, N, H, d), dtype=torch.uint8, device=q.device)
+    k8 = torch.empty((B, N, Hkv, d), dtype=torch.uint8, device=q.device)
+    v8 = torch.empty((B, N, Hkv, d), dtype=torch.uint8, device=q.device)
+    qs = torch.empty((B, H, nblk), dtype=torch.float32, device=q.device)
+    ks = torch.empty((B, Hkv, nblk), dtype=torch.float32, device=q.device)
+    vs = torch.empty((B, Hkv, nblk), dtype=torch.float32, device=q.device)
+    rc = library().attn_fp8_prep_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(q8), _ptr(k8), _ptr(v8), _ptr(qs), _ptr(ks),
+                                     _ptr(vs), B, H, Hkv, N, d, int(mode), int(sign_seed) & 0xFFFFFFFFFFFFFFFF,
+                                     ctypes.c_void_p(_stream(stream)))
+    _check("attn_fp8_prep_qkv", rc)
+    return q8, k8, v8, qs, ks, vs
+
+
 def fp8_prepare_qkv(q, k, v, mode: int = MODE_BLOCK_HADAMARD, sign_seed: int = 0, stream=None, rope=None):
-    """Runs the prep on Q, K (rotated in mode 1) and V (never rotated).
+    """Runs the prep on Q, K (rotated in mode 1) and V (never rotated), one
+    launch where the library has it (attn_fp8_prep_qkv).
     rope: optional (cos, sin, interleaved); RoPE is then fused into the prep
     of Q and K."""
     if rope is None:
-        q8, qs = attn_fp8_prep(q, mode, sign_seed, False, stream=stream)
-        k8, ks = attn_fp8_prep(k, mode, sign_seed, False, stream=stream)
+        return attn_fp8_prep_qkv(q, k, v, mode, sign_seed, stream=stream)
     else:
         c, s_, il = rope
         q8, qs = attn_fp8_prep_rope(q, c, s_, mode, sign_seed, il, stream=stream)

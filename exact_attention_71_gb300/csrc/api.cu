@@ -148,6 +148,43 @@ int prep_launch(const void* x, int B, int H, int N, int d, CUtensorMap* map, att
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The tensor-core prep (modes 0 and 1 at d = 64 and 128) of up to three bf16
+// (B, N, H_i, d) tensors in one launch: x[i] -> codes x8[i], block scales
+// scales[i]; rotate[i] = 1 multiplies tensor i by diag(+-1) x Hadamard.
+int prep_tc(int n, const void* const* x, void* const* x8, float* const* scales, const int* Hs, const int* rotate,
+            int B, int N, int d, unsigned long long sign_seed, cudaStream_t stream) {
+    CUtensorMap maps[3];
+    attn::PrepTcParams p{};
+    p.N = N;
+    p.nblk = (N + 127) / 128;
+    long long total = 0;
+    for (int i = 0; i < 3; ++i) {
+        const int src = i < n ? i : 0;     // unused slots repeat tensor 0's map, with no blocks
+        int rc = make_map(&maps[i], x[src], B, Hs[src], N, d, 2, 128, 128);
+        if (rc != ATTN_OK) return rc;
+        p.t[i].x8 = static_cast<uint8_t*>(x8[src]);
+        p.t[i].scales = scales[src];
+        p.t[i].H = Hs[src];
+        p.t[i].rotate = rotate[src];
+        const long long blocks = i < n ? static_cast<long long>(B) * Hs[i] * p.nblk : 0;
+        p.t[i].blocks = static_cast<int>(blocks);
+        total += blocks;
+    }
+    if (total >= (1ll << 31)) return fail(ATTN_ERR_INVALID_ARG, "problem too large for one launch");
+    p.total_blocks = static_cast<int>(total);
+    p.seed = sign_seed;
+    attn::PrepLaunch L;
+    int rc = sm_count(&L.num_sms);
+    if (rc != ATTN_OK) return rc;
+    if ((rc = status_ptr(&L.status)) != ATTN_OK) return rc;
+    L.wait_limit = g_wait_limit.load();
+    p.wait_limit = L.wait_limit;
+    p.status = L.status;
+    cudaError_t e = attn::run_fp8_prep_tc(maps, p, d, L, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "FP8 prep launch");
+    return ATTN_OK;
+}
+
 int check_common(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H, int N,
                  int d, int window) {
     if (B < 0 || H < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d N=%d)", B, H, N);
@@ -292,6 +329,11 @@ int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, i
     if (!x || !x8 || !scales) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(x) || !aligned16(x8) || !aligned16(scales))
         return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if ((mode == 0 || mode == 1) && d <= 128) {
+        // The rotation as a tensor-core product.
+        const int rot = (mode == 1 && !is_v) ? 1 : 0;
+        return prep_tc(1, &x, &x8, &scales, &H, &rot, B, N, d, sign_seed, static_cast<cudaStream_t>(stream));
+    }
     CUtensorMap map;
     attn::PrepLaunch L;
     int rc = prep_launch(x, B, H, N, d, &map, &L);
@@ -300,6 +342,37 @@ int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, i
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_fp8_prep launch");
     return ATTN_OK;
+}
+
+int attn_fp8_prep_qkv(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8, float* q_scale,
+                      float* k_scale, float* v_scale, int B, int H, int H_kv, int N, int d, int mode,
+                      unsigned long long sign_seed, void* stream) {
+    g_err[0] = '\0';
+    if (B < 0 || H < 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "negative size (B=%d H=%d N=%d)", B, H, N);
+    if (d != 64 && d != 128 && d != 256) return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128, 256)", d);
+    if (mode < 0 || mode > 2) return fail(ATTN_ERR_INVALID_ARG, "mode %d (0, 1 or 2)", mode);
+    if (H_kv <= 0 || H % H_kv != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "key/value heads (%d) must divide query heads (%d)", H_kv, H);
+    if (static_cast<long long>(B) * H * N == 0) return ATTN_OK;
+    const void* x[3] = {q, k, v};
+    void* x8[3] = {q8, k8, v8};
+    float* sc[3] = {q_scale, k_scale, v_scale};
+    for (int i = 0; i < 3; ++i) {
+        if (!x[i] || !x8[i] || !sc[i]) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+        if (!aligned16(x[i]) || !aligned16(x8[i]) || !aligned16(sc[i]))
+            return fail(ATTN_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    }
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((mode == 0 || mode == 1) && d <= 128) {
+        const int Hs[3] = {H, H_kv, H_kv};
+        const int rot[3] = {mode == 1 ? 1 : 0, mode == 1 ? 1 : 0, 0};
+        return prep_tc(3, x, x8, sc, Hs, rot, B, N, d, sign_seed, s);
+    }
+    // Head dim 256 and the per-tensor mode: one launch per tensor.
+    int rc = attn_fp8_prep(q, q8, q_scale, B, H, N, d, 128, mode, sign_seed, 0, stream);
+    if (rc == ATTN_OK) rc = attn_fp8_prep(k, k8, k_scale, B, H_kv, N, d, 128, mode, sign_seed, 0, stream);
+    if (rc == ATTN_OK) rc = attn_fp8_prep(v, v8, v_scale, B, H_kv, N, d, 128, mode, sign_seed, 1, stream);
+    return rc;
 }
 
 int attn_fp8_prep_rope(const void* x, void* x8, float* scales, const float* rope_cos, const float* rope_sin,
@@ -713,14 +786,9 @@ int attn_fwd_fp8_host(const void* q, const void* k, const void* v, void* o, floa
                              float* qs = reinterpret_cast<float*>(base + soff[3]);
                              float* ks = reinterpret_cast<float*>(base + soff[4]);
                              float* vs = reinterpret_cast<float*>(base + soff[5]);
-                             int r = attn_fp8_prep(base + L.in_off[0], base + soff[0], qs, nb, H, N, d, 128, mode,
-                                                   sign_seed, 0, s);
-                             if (r == ATTN_OK)
-                                 r = attn_fp8_prep(base + L.in_off[1], base + soff[1], ks, nb, H_kv, N, d, 128, mode,
-                                                   sign_seed, 0, s);
-                             if (r == ATTN_OK)
-                                 r = attn_fp8_prep(base + L.in_off[2], base + soff[2], vs, nb, H_kv, N, d, 128, mode,
-                                                   sign_seed, 1, s);
+                             int r = attn_fp8_prep_qkv(base + L.in_off[0], base + L.in_off[1], base + L.in_off[2],
+                                                       base + soff[0], base + soff[1], base + soff[2], qs, ks, vs, nb,
+                                                       H, H_kv, N, d, mode, sign_seed, s);
                              if (r != ATTN_OK) return r;
                              return launch_forward(true, base + soff[0], base + soff[1], base + soff[2],
                                                    base + L.out_off[0], reinterpret_cast<float*>(base + L.out_off[1]),

@@ -31,16 +31,6 @@ namespace {
 
 constexpr int kBlockRows = 128;
 
-// Sign c of the +-1 diagonal: bit 63 of splitmix64 output c for state
-// `seed` (output c is the mixing function applied to seed + (c + 1) * gamma).
-__device__ __forceinline__ float diag_sign(unsigned long long seed, int c) {
-    unsigned long long z = seed + static_cast<unsigned long long>(c + 1) * 0x9E3779B97F4A7C15ull;
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    z ^= z >> 31;
-    return (z >> 63) ? -1.0f : 1.0f;
-}
-
 enum Pass { kFused = 0, kAmaxOnly = 1, kApplyScale = 2 };
 constexpr int kSitePrepLoad = 0x91;   // status site: the prep gave up waiting for a tile
 enum Rope { kNoRope = 0, kRopeHalf = 1, kRopeInterleaved = 2 };
@@ -65,18 +55,6 @@ __device__ __forceinline__ void load_floats(const float* __restrict__ p, float (
 #pragma unroll
         for (int k = 0; k < K; ++k) out[k] = f[k];
     }
-}
-
-// x / s rounded to nearest for s > 0, from the correctly rounded reciprocal
-// and one residual correction (Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. R&D 1990): with
-// inv = RN(1/s), q0 = RN(x * inv) and the exact residual x - q0 * s (one FMA),
-// q0 + residual * inv rounds to RN(x / s) for the normal-range quotients
-// here (|x / s| <= 448).  The sign is copied so that -0 / s stays -0.
-__device__ __forceinline__ float div_by_scale(float x, float s, float inv) {
-    const float q0 = x * inv;
-    const float rem = fmaf(-q0, s, x);
-    return copysignf(fmaf(rem, inv, q0), x);
 }
 
 template <int E> struct RowLoad;

@@ -131,11 +131,33 @@ int attn_fwd_fp8_gqa(const void* q8, const void* k8, const void* v8, void* o, fl
  *   is_v   : nonzero for V (never rotated).
  * scale = amax / 448 of the block (1 for an all-zero block); each element is
  * r / scale rounded to nearest-even e4m3 and saturated to +-448.  amax, the
- * scale and the division are float32.
+ * scale and the division are float32.  For modes 0 and 1 at d = 64 and 128
+ * the product x (D H) is taken on the tensor cores (D H is a +-1 matrix,
+ * exact in bf16; fp32 accumulation), so r may differ from a float32
+ * butterfly evaluation in its last bits.
  */
 int attn_fp8_prep(const void* x, void* x8, float* scales, int B, int H, int N, int d,
                   int block_rows, int mode, unsigned long long sign_seed, int is_v,
                   void* stream);
+
+/*
+ * attn_fp8_prep_qkv -- attn_fp8_prep of Q, K and V of one attention call in
+ * one launch (deep-reading report §2.2 / §3.3): Q and K rotated in mode 1
+ * (the same sign_seed, so Q K^T is unchanged), V never rotated.
+ *   q          : const bf16 (B, N, H, d);  k, v : const bf16 (B, N, H_kv, d)
+ *   q8, k8, v8 : e4m3, the same shapes, written
+ *   q_scale    : float32 (B, H, ceil(N / 128)); k_scale, v_scale : (B, H_kv,
+ *                ceil(N / 128)); written
+ *   mode, sign_seed : as attn_fp8_prep (block_rows is 128).
+ * H_kv must divide H.  Modes 0 and 1 at d = 64 and 128 run as one launch
+ * over the blocks of all three tensors; d = 256 and mode 2 run as three
+ * attn_fp8_prep calls.  Results are those of three attn_fp8_prep calls.
+ * Errors: ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED as attn_fp8_prep,
+ * before any launch.
+ */
+int attn_fp8_prep_qkv(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8,
+                      float* q_scale, float* k_scale, float* v_scale, int B, int H, int H_kv,
+                      int N, int d, int mode, unsigned long long sign_seed, void* stream);
 
 /*
  * attn_fp8_prep_rope -- rotary position embedding fused with the FP8 prep of

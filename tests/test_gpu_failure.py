@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 ATTN_ERR_DEVICE_TIMEOUT = -4
 FWD_SITES = {0x11, 0x12, 0x21, 0x22, 0x23, 0x24, 0x31, 0x32, 0x41}
 BWD_SITES = {0x51, 0x52, 0x61, 0x62, 0x63, 0x64, 0x65, 0x66, 0x71, 0x72, 0x73, 0x74, 0x81, 0x82}
-PREP_SITES = {0x91}
+PREP_SITES = {0x91, 0x92, 0x93, 0x94}   # CUDA-core prep load; tensor-core prep load, MMA, producer
 KNOWN_SITES = FWD_SITES
 
 
@@ -85,8 +85,10 @@ def test_backward_wait_timeout_is_reported_and_the_context_survives():
     assert float((got[0].float() - want[0].float()).abs().max()) <= 1e-2 * float(want[0].float().abs().max())
 
 
-def test_prep_wait_timeout_is_reported_and_the_context_survives():
-    x = synth.tensor_bf16((2, 4096, 4, 128), seed=3, stream=1)
+@pytest.mark.parametrize("d", [128, 256])
+def test_prep_wait_timeout_is_reported_and_the_context_survives(d):
+    """d = 128 runs the tensor-core prep, d = 256 the CUDA-core one."""
+    x = synth.tensor_bf16((2, 4096, 4, d), seed=3, stream=1)
     xd = to_dev(x)
     want = api.attn_fp8_prep(xd, mode=api.MODE_BLOCK_HADAMARD, sign_seed=7)
     torch.cuda.synchronize()
@@ -113,3 +115,20 @@ def test_fp8_head_dim_256_wait_timeout_is_reported_and_the_context_survives():
     torch.cuda.synchronize()
     assert torch.equal(got.view(torch.int16), want.view(torch.int16)) and torch.equal(got_lse, want_lse)
     assert api.device_status()[0] == 0
+
+
+def test_fused_qkv_prep_wait_timeout_is_reported_and_the_context_survives():
+    B, N, H, Hkv, d = 2, 2048, 4, 2, 128
+    q = to_dev(synth.tensor_bf16((B, N, H, d), seed=5, stream=1))
+    k = to_dev(synth.tensor_bf16((B, N, Hkv, d), seed=5, stream=2))
+    v = to_dev(synth.tensor_bf16((B, N, Hkv, d), seed=5, stream=3))
+    want = api.attn_fp8_prep_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, 11)
+    torch.cuda.synchronize()
+    rc, site = _timeout_then_recover(lambda: api.attn_fp8_prep_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, 11))
+    assert rc in (0, ATTN_ERR_DEVICE_TIMEOUT), rc
+    if rc != 0:
+        assert site in PREP_SITES, hex(site)
+    got = api.attn_fp8_prep_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, 11)
+    torch.cuda.synchronize()
+    for a, b in zip(got, want):
+        assert torch.equal(a, b)

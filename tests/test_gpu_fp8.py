@@ -52,16 +52,12 @@ import torch
 
 import oracle
 from exact_attention_71_gb300 import api, synth
-from tests.helpers import FP8_LSE, FP8_RMS, bf16_half_ulp, gpu_rows, lse_rows, to_dev
+from tests.helpers import (FP8_LSE, FP8_RMS, assert_codes_match_up_to_midpoints, bf16_half_ulp, gpu_rows,
+                           lse_rows, to_dev)
 
 pytestmark = pytest.mark.gpu
 
 SEED = 1234
-
-
-def _e4m3_midpoints():
-    vals = np.unique(np.abs(oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))))
-    return (vals[:-1] + vals[1:]) / 2
 
 
 def _prep_gpu(x_bits, mode, is_v):
@@ -82,30 +78,53 @@ def test_prep_bit_exact_without_rotation(shape, mode, is_v):
 
 @pytest.mark.parametrize("shape", [(1, 300, 2, 64), (2, 256, 3, 128), (1, 130, 2, 256)])
 def test_prep_hadamard_codes(shape):
+    """Mode 1 codes against the oracle up to rounding midpoints (d = 64 and
+    128 rotate on the tensor cores, d = 256 with float32 butterflies)."""
     x = synth.tensor_bf16(shape, seed=3, stream=2, outliers=True)
     c_gpu, s_gpu = _prep_gpu(x, api.MODE_BLOCK_HADAMARD, False)
     c_ref, s_ref, rot = oracle.fp8_quantize(x, oracle.MODE_BLOCK_HADAMARD, seed=SEED, return_rotated=True)
     np.testing.assert_allclose(s_gpu, s_ref, rtol=2e-6, atol=0)
-    # exact quotient of the oracle (double) and its distance to a midpoint
-    nblk = s_ref.shape[2]
-    B, N, H, d = shape
-    sc = np.repeat(s_ref.transpose(0, 2, 1), 128, axis=1)[:, :N]            # (B, N, H)
-    y = rot.astype(np.float64) / sc[..., None]
-    mids = _e4m3_midpoints()
-    a = np.abs(y).ravel()
-    pos = np.searchsorted(mids, a)
-    near = np.minimum(np.abs(a - mids[np.clip(pos - 1, 0, len(mids) - 1)]),
-                      np.abs(a - mids[np.clip(pos, 0, len(mids) - 1)])) <= 1e-5 * np.maximum(a, 2.0 ** -9)
-    cg, cr = c_gpu.ravel(), c_ref.ravel()
-    same = cg == cr
-    assert np.all(same | near), f"{np.sum(~(same | near))} codes differ away from a rounding midpoint"
-    # where they differ at a midpoint, the GPU code is a neighbour of the oracle's
-    diff = ~same
-    mg, mr = (cg[diff] & 0x7F).astype(int), (cr[diff] & 0x7F).astype(int)
-    same_sign = (cg[diff] & 0x80) == (cr[diff] & 0x80)
-    adjacent = (np.abs(mg - mr) == 1) & (same_sign | (np.minimum(mg, mr) == 0))
-    assert np.all(adjacent)
-    assert diff.mean() < 1e-3
+    assert_codes_match_up_to_midpoints(c_gpu, c_ref, s_ref, rot, x=synth.bf16_bits_to_f32(x).astype(np.float64))
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_prep_qkv_in_one_call_equals_three_single_tensor_calls(d, mode):
+    """attn_fp8_prep_qkv (one launch over Q, K and V for modes 0 and 1 at
+    d <= 128) gives the codes and scales of three attn_fp8_prep calls, bit for
+    bit: grouped-query heads, a ragged last block, several batches."""
+    B, N, H, Hkv = 2, 300, 4, 2
+    q = synth.tensor_bf16((B, N, H, d), seed=4, stream=1, outliers=True)
+    k = synth.tensor_bf16((B, N, Hkv, d), seed=4, stream=2, outliers=True)
+    v = synth.tensor_bf16((B, N, Hkv, d), seed=4, stream=3, outliers=True)
+    got = api.attn_fp8_prep_qkv(to_dev(q), to_dev(k), to_dev(v), mode, SEED)
+    want = [api.attn_fp8_prep(to_dev(x), mode=mode, sign_seed=SEED, is_v=is_v)
+            for x, is_v in ((q, False), (k, False), (v, True))]
+    torch.cuda.synchronize()
+    for i, name in enumerate("qkv"):
+        assert torch.equal(got[i], want[i][0]), name
+        assert torch.equal(got[3 + i], want[i][1]), name
+    assert api.device_status()[0] == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prep_full_size_codes_against_oracle(d):
+    """The C4-size tensor (B=2, N=8192, 16 heads at d=128; hidden 2048 at
+    d=64) through the one-launch prep: K's codes against the oracle (up to
+    rounding midpoints) and V's bit for bit."""
+    B, N, H = 2, 8192, 2048 // d // (2 if d == 64 else 1)
+    k = synth.tensor_bf16((B, N, H, d), seed=0, stream=2, outliers=True)
+    v = synth.tensor_bf16((B, N, H, d), seed=0, stream=3, outliers=True)
+    kd, vd = to_dev(k), to_dev(v)
+    _, k8, v8, _, ks, vs = api.attn_fp8_prep_qkv(kd, kd, vd, api.MODE_BLOCK_HADAMARD, SEED)
+    torch.cuda.synchronize()
+    c_ref, s_ref, rot = oracle.fp8_quantize(k, oracle.MODE_BLOCK_HADAMARD, seed=SEED, return_rotated=True)
+    np.testing.assert_allclose(ks.cpu().numpy(), s_ref, rtol=2e-6, atol=0)
+    assert_codes_match_up_to_midpoints(k8.cpu().numpy(), c_ref, s_ref, rot,
+                                       x=synth.bf16_bits_to_f32(k).astype(np.float64))
+    cv_ref, sv_ref = oracle.fp8_quantize(v, oracle.MODE_BLOCK_HADAMARD, seed=SEED, is_v=True)
+    np.testing.assert_array_equal(vs.cpu().numpy(), sv_ref)
+    np.testing.assert_array_equal(v8.cpu().numpy(), cv_ref)
 
 
 def test_prep_zero_block_and_ragged_tail():
