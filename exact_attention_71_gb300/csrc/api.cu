@@ -248,6 +248,7 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
     if ((rc = make_map(&maps.q, q, B, H, N, d, g.elem_bytes, 128, g.swizzle)) != ATTN_OK) return rc;
     if ((rc = make_map(&maps.k, k, B, Hkv, N, d, g.elem_bytes, g.bn, g.swizzle)) != ATTN_OK) return rc;
     if ((rc = make_map(&maps.v, v, B, Hkv, N, d, g.elem_bytes, g.bn, g.swizzle)) != ATTN_OK) return rc;
+    if ((rc = make_map(&maps.o, o, B, H, N, d, 2, 32, 128)) != ATTN_OK) return rc;
     attn::FwdParams p{};
     p.o = o;
     p.lse = lse;

@@ -17,6 +17,11 @@
 //                     in shared memory) and O_t += P_t V_j (P from tensor
 //                     memory, V from shared memory), completion signalled
 //                     with tcgen05.commit
+// For d >= 128, O leaves through shared memory: each softmax warp owns a
+// 4 KB slot (its 32 rows x one 128-byte column box, 128-byte swizzled) and
+// hands every box to a TMA store, so the epilogue costs a few shared-memory
+// wavefronts per box instead of one scattered global store per row and 16
+// bytes.  At d = 64 (one box per row) the direct row stores measured faster.
 // Tensor memory (512 columns x 128 lanes of fp32):
 //   S_t at columns [128 t, 128 t + BN); P_t (bf16 pairs or e4m3 quads)
 //   overwrites the first columns of S_t; O_t at columns [256 + D t, ...).
@@ -34,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "sm103_bulk.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -105,6 +111,11 @@ struct FwdCfg {
     static constexpr int MMA_WARPS = (!FP8 && D == 128 && NQ == 2) ? 2 : 1;
     static constexpr int THREADS = NQ * 128 + 128;
     static constexpr int BAR_BYTES = 256;
+    // Output staging (O_VIA_TMA): one slot of 32 rows x 128 bytes per
+    // softmax warp.
+    static constexpr bool O_VIA_TMA = D >= 128;
+    static constexpr int EPI_SLOT_BYTES = 32 * 128;
+    static constexpr int EPI_BYTES = O_VIA_TMA ? NQ * 4 * EPI_SLOT_BYTES : 0;
     // The reference maximum of a row moves only when the row maximum exceeds
     // it by more than this (log2 units), so P <= 2^RESCALE_LOG2.  FP8 scales P
     // by P8_SCALE = 16 before the e4m3 cast: P * P8_SCALE <= 2^4.8 * 16 ~ 445.7
@@ -123,7 +134,7 @@ struct FwdCfg {
     static constexpr int HIGH_REGS_RAW = ((LAUNCH_REGS * THREADS - LOW_REGS * 128) / (NQ * 128)) / 8 * 8;
     static constexpr int HIGH_REGS = HIGH_REGS_RAW > 248 ? 248 : HIGH_REGS_RAW;
     static_assert(HIGH_REGS * NQ * 128 + LOW_REGS * 128 <= LAUNCH_REGS * THREADS, "register split");
-    static constexpr int SMEM_BYTES = 1024 + NQ * Q_TILE_BYTES + NSTAGE * STAGE_BYTES + BAR_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + NQ * Q_TILE_BYTES + NSTAGE * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
 
     static_assert(D == 64 || D == 128 || D == 256, "head_dim");
     static_assert(BN == 64 || BN == 128, "key tile");
@@ -284,13 +295,16 @@ __device__ __forceinline__ bool key_in_tile(const WorkItem<Cfg::NQ>& w, int t, i
 // Next key tile after u in the union of the active tiles' sets, or -1.
 template <class Cfg>
 __device__ __forceinline__ int next_key(const WorkItem<Cfg::NQ>& w, int u) {
-    if constexpr (!Cfg::SPARSE) return u < w.u_hi ? u + 1 : -1;
-    for (int x = u + 1; x <= w.u_hi; ++x) {
+    if constexpr (!Cfg::SPARSE) {
+        return u < w.u_hi ? u + 1 : -1;
+    } else {
+        for (int x = u + 1; x <= w.u_hi; ++x) {
 #pragma unroll
-        for (int t = 0; t < Cfg::NQ; ++t)
-            if (w.active[t] && key_in_tile<Cfg>(w, t, x)) return x;
+            for (int t = 0; t < Cfg::NQ; ++t)
+                if (w.active[t] && key_in_tile<Cfg>(w, t, x)) return x;
+        }
+        return -1;
     }
-    return -1;
 }
 
 // One query tile's part of an item, for roles that index the tile at run
@@ -313,10 +327,13 @@ __device__ __forceinline__ TileKeys tile_keys(const WorkItem<Cfg::NQ>& w, int t)
 // Next key tile after u in the tile's set, or -1.
 template <class Cfg>
 __device__ __forceinline__ int next_in(const TileKeys& k, int u) {
-    if constexpr (!Cfg::SPARSE) return u < k.last ? u + 1 : -1;
-    for (int x = u + 1; x <= k.last; ++x)
-        if (__ldg(k.mrow + ((x * Cfg::BN) >> 7)) != 0) return x;
-    return -1;
+    if constexpr (!Cfg::SPARSE) {
+        return u < k.last ? u + 1 : -1;
+    } else {
+        for (int x = u + 1; x <= k.last; ++x)
+            if (__ldg(k.mrow + ((x * Cfg::BN) >> 7)) != 0) return x;
+        return -1;
+    }
 }
 
 template <class Cfg>
@@ -357,34 +374,19 @@ __device__ __forceinline__ WorkItem<Cfg::NQ> decode_item(const FwdParams& p, int
     return w;
 }
 
-// MMA issue order (the ping-pong of the two query tiles): an item's steps
-// u = u_lo .. (its last key tile) + 1 in walk order and, within a step, t =
-// 0, 1; the block (t, u) holds O_t += P_t V_{u-1} (when key tile u-1 is in
-// tile t's set) and S_t = Q_t K_u^T (when u is); empty blocks are skipped.
-// With two issuers each waits for its blocks' turns in this order.  Dense
-// walks are contiguous, so a block's position has a closed form
-// (blocks_before, plus the blocks of the CTA's earlier items); sparse walks
-// are not, so there both issuers walk every step and count every non-empty
-// block (a running count across items).
-template <int NQ>
-__device__ __forceinline__ int blocks_before(const WorkItem<NQ>& w, int t, int u) {
-    int n = 0;
-#pragma unroll
-    for (int x = 0; x < NQ; ++x)
-        if (w.active[x]) n += min(max(u - w.lo[x], 0), w.hi[x] - w.lo[x] + 2);
-    if (NQ > 1 && t == 1 && w.active[0] && u >= w.lo[0] && u <= w.hi[0] + 1) ++n;
-    return n;
-}
-
-template <int NQ>
-__device__ __forceinline__ int item_blocks(const WorkItem<NQ>& w) {
-    int n = 0;
-#pragma unroll
-    for (int x = 0; x < NQ; ++x)
-        if (w.active[x]) n += w.hi[x] - w.lo[x] + 2;
-    return n;
-}
-
+// Key-tile walk and MMA issue order (the ping-pong of the two query tiles).
+// A CTA walks the steps of its items back to back: one step per key tile u
+// of an item (walk order), and one final step after its last item.  A step's
+// ring stage holds K_u and the V of the previous step's key tile (which may
+// belong to the previous item), and its block for tile t (t = 0, 1 in
+// order) holds O_t += P_t V of the previous step (when tile t had an S
+// there) followed by S_t = Q_t K_u^T (when u is in tile t's set).  So the
+// last P V of one item and the first S of the next share a step, like any
+// two consecutive key tiles: the next item's first S of a tile never waits
+// for the other tile's last softmax of the previous item, and an item costs
+// no extra step for its final P V.  Empty blocks are skipped; the issuers
+// count the non-empty blocks and, with two issuers, each waits for its
+// blocks' turns in that order.
 // Bounded wait (whole warp) until `k` MMA blocks have been issued.
 __device__ __forceinline__ bool wait_turn(volatile int* issued, int k, volatile int* abort_flag,
                                           const FwdParams& p, int site) {
@@ -445,14 +447,16 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                    const __grid_constant__ CUtensorMap tmap_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                    const FwdParams p) {
     constexpr int D = Cfg::D, BN = Cfg::BN, NQ = Cfg::NQ, BM = Cfg::BM, NSTAGE = Cfg::NSTAGE;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;                                       // NQ x Q tile
     uint8_t* sKV = smem + NQ * Cfg::Q_TILE_BYTES;             // NSTAGE x (K tile, V tile)
-    SharedBarriers* bars = reinterpret_cast<SharedBarriers*>(sKV + NSTAGE * Cfg::STAGE_BYTES);
+    uint8_t* sEpi = sKV + NSTAGE * Cfg::STAGE_BYTES;        // 4*NQ output slots
+    SharedBarriers* bars = reinterpret_cast<SharedBarriers*>(sEpi + Cfg::EPI_BYTES);
     volatile int* abort_flag = &bars->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -481,6 +485,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
         tma_prefetch_desc(&tmap_v);
+        tma_prefetch_desc(&tmap_o);
     }
     if (warp == 0) {
         tmem_alloc(&bars->tmem_base, Cfg::TMEM_COLS);
@@ -503,10 +508,36 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t qn[NQ];
 #pragma unroll
             for (int t = 0; t < NQ; ++t) qn[t] = 0;
+            int vb = 0, vh = 0, vu = -1;   // V of the previous step (batch, key/value head, key tile)
+            // One ring step: K tile ku of (batch kb, key/value head kh) when
+            // with_k, and the previous step's V when there is one.
+            auto load_step = [&](bool with_k, int kb, int kh, int ku) -> bool {
+                const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
+                if (!wait_phase(&bars->ring_empty[stage], (round & 1) ^ 1, abort_flag, p, SITE_LOAD_EMPTY))
+                    return false;
+                const bool with_v = vu >= 0;
+                mbar_arrive_expect_tx(&bars->ring_full[stage],
+                                      (with_k ? Cfg::KV_TILE_BYTES : 0) + (with_v ? Cfg::KV_TILE_BYTES : 0));
+                uint8_t* dst = sKV + stage * Cfg::STAGE_BYTES;
+                if (with_k) {
+#pragma unroll
+                    for (int cb = 0; cb < Cfg::NCB; ++cb)
+                        tma_load_4d(dst + cb * (BN * Cfg::SW), &tmap_k, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS,
+                                    kh, ku * BN, kb, pol_kv);
+                }
+                if (with_v) {
+#pragma unroll
+                    for (int cb = 0; cb < Cfg::NCB; ++cb)
+                        tma_load_4d(dst + Cfg::KV_TILE_BYTES + cb * (BN * Cfg::SW), &tmap_v, &bars->ring_full[stage],
+                                    cb * Cfg::BOX_ELEMS, vh, vu * BN, vb, pol_kv);
+                }
+                ++it;
+                return true;
+            };
             bool ok = true;
             for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
-            const int item = round_item(rnd);
-            if (item >= total_items) continue;
+                const int item = round_item(rnd);
+                if (item >= total_items) continue;
                 const WorkItem<NQ> w = decode_item<Cfg>(p, item);
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
@@ -523,35 +554,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tma_load_4d(sQ + t * Cfg::Q_TILE_BYTES + cb * (BM * Cfg::SW), &tmap_q, &bars->q_full[t],
                                     cb * Cfg::BOX_ELEMS, w.h, w.q0 + t * BM, w.b, pol_q);
                 }
-                // Steps over the item's key tiles u (in order) and one more:
-                // each loads K_u (while there is a u) and V of the previous u.
-                for (int u = w.u_lo, prev = -1; ok && (u >= 0 || prev >= 0);) {
-                    const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
-                    if (!wait_phase(&bars->ring_empty[stage], (round & 1) ^ 1, abort_flag, p, SITE_LOAD_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    const bool with_k = u >= 0, with_v = prev >= 0;
-                    mbar_arrive_expect_tx(&bars->ring_full[stage],
-                                          (with_k ? Cfg::KV_TILE_BYTES : 0) + (with_v ? Cfg::KV_TILE_BYTES : 0));
-                    uint8_t* dst = sKV + stage * Cfg::STAGE_BYTES;
-                    if (with_k) {
-#pragma unroll
-                        for (int cb = 0; cb < Cfg::NCB; ++cb)
-                            tma_load_4d(dst + cb * (BN * Cfg::SW), &tmap_k, &bars->ring_full[stage], cb * Cfg::BOX_ELEMS,
-                                        w.h / p.group, u * BN, w.b, pol_kv);
-                    }
-                    if (with_v) {
-#pragma unroll
-                        for (int cb = 0; cb < Cfg::NCB; ++cb)
-                            tma_load_4d(dst + Cfg::KV_TILE_BYTES + cb * (BN * Cfg::SW), &tmap_v, &bars->ring_full[stage],
-                                        cb * Cfg::BOX_ELEMS, w.h / p.group, prev * BN, w.b, pol_kv);
-                    }
-                    ++it;
-                    prev = u;
-                    u = u >= 0 ? next_key<Cfg>(w, u) : -1;
+                // The item's steps: K_u, and the V of the previous step.
+                const int kh = w.h / p.group;
+                for (int u = w.u_lo; ok && u >= 0; u = next_key<Cfg>(w, u)) {
+                    ok = load_step(true, w.b, kh, u);
+                    vb = w.b;
+                    vh = kh;
+                    vu = u;
                 }
             }
+            // Final step: the V of the last key tile.
+            if (ok && vu >= 0) ok = load_step(false, 0, 0, 0);
             // Let every copy this warp issued land before the CTA can exit (on
             // the normal path these phases have completed already).
             const uint32_t first = it > NSTAGE ? it - NSTAGE : 0;
@@ -585,92 +598,92 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             qdesc[t] = sdesc_swz<Cfg::SW>(smem_u32(sQ) + t * Cfg::Q_TILE_BYTES, 16, 8 * Cfg::SW);
         uint32_t it = 0;
         uint32_t pv_count[NQ], qn[NQ];
+        // Bit t: tile t's P V of the previous step is due (pend), accumulates
+        // into O_t (pend_acc: not the tile's first key tile of its item) and
+        // ends the tile's item (pend_last: O_t is final once it is done).
+        uint32_t pend = 0, pend_acc = 0, pend_last = 0;
 #pragma unroll
         for (int t = 0; t < NQ; ++t) pv_count[t] = qn[t] = 0;
-        int item_base = 0;   // dense: blocks of the CTA's earlier items
-        int turn = 0;        // sparse: non-empty blocks (of both issuers) so far
+        int turn = 0;        // non-empty blocks (of both issuers) so far
+        // One step.  Bit t of s_mask: tile t has S = Q_t K^T here; of
+        // first_mask / last_mask: that key tile is the tile's first / last of
+        // its item (all 0 for the final step).
+        auto mma_step = [&](uint32_t s_mask, uint32_t first_mask, uint32_t last_mask) -> bool {
+            const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
+            ++it;
+            if (!warp_wait(&bars->ring_full[stage], round & 1, abort_flag, p, SITE_MMA_FULL)) return false;
+            const uint32_t st_addr = sKV_addr + stage * Cfg::STAGE_BYTES;
+            const uint64_t kdesc = sdesc_swz<Cfg::SW>(st_addr, 16, 8 * Cfg::SW);
+            const uint64_t vdesc = sdesc_swz<Cfg::SW>(st_addr + Cfg::KV_TILE_BYTES, BN * Cfg::SW, 8 * Cfg::SW);
+            bool issued_any = false;
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) {
+                const bool do_pv = (pend >> t) & 1u;
+                const bool do_s = (s_mask >> t) & 1u;
+                if (!do_pv && !do_s) continue;
+                const int k = turn++;
+                if (t % MW != wi) continue;
+                if (do_pv && !warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) return false;
+                if (MW > 1 && !wait_turn(issued, k, abort_flag, p, SITE_TURN)) return false;
+                tc_fence_after();
+                if (elect_one()) {
+                    if (do_pv) {
+                        issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc, (pend_acc >> t) & 1u);
+                        if ((pend_last >> t) & 1u) mma_commit(&bars->o_full[t]);
+                    }
+                    if (do_s) {
+                        issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
+                        mma_commit(&bars->s_full[t]);
+                        // Q_t is free for the next item once its last S MMA is done.
+                        if ((last_mask >> t) & 1u) mma_commit(&bars->q_empty[t]);
+                    }
+                    if (MW > 1) {
+                        __threadfence_block();
+                        *issued = k + 1;
+                    }
+                }
+                __syncwarp();
+                issued_any = true;
+                if (do_pv) ++pv_count[t];
+            }
+            pend = s_mask;
+            pend_acc = s_mask & ~first_mask;
+            pend_last = s_mask & last_mask;
+            // This issuer is done with the stage once its MMAs of the step are.
+            if (elect_one()) {
+                if (issued_any) mma_commit(&bars->ring_empty[stage]);
+                else mbar_arrive(&bars->ring_empty[stage]);
+            }
+            __syncwarp();
+            return true;
+        };
         bool ok = true;
+        bool any_step = false;
         for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
             const int item = round_item(rnd);
             if (item >= total_items) continue;
             const WorkItem<NQ> w = decode_item<Cfg>(p, item);
-            bool first_pv[NQ];
 #pragma unroll
             for (int t = 0; t < NQ; ++t) {
-                first_pv[t] = true;
                 if (t % MW == wi && w.active[t] && ok) {
                     ok = warp_wait(&bars->q_full[t], qn[t] & 1, abort_flag, p, SITE_MMA_Q);
                     ++qn[t];
                 }
             }
-            for (int u = w.u_lo, prev = -1; ok && (u >= 0 || prev >= 0); prev = u, u = u >= 0 ? next_key<Cfg>(w, u) : -1) {
-                const uint32_t stage = it % NSTAGE, round = it / NSTAGE;
-                ++it;
-                if (!warp_wait(&bars->ring_full[stage], round & 1, abort_flag, p, SITE_MMA_FULL)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t st_addr = sKV_addr + stage * Cfg::STAGE_BYTES;
-                const uint64_t kdesc = sdesc_swz<Cfg::SW>(st_addr, 16, 8 * Cfg::SW);
-                const uint64_t vdesc = sdesc_swz<Cfg::SW>(st_addr + Cfg::KV_TILE_BYTES, BN * Cfg::SW, 8 * Cfg::SW);
-                bool issued_any = false;
+            for (int u = w.u_lo; ok && u >= 0; u = next_key<Cfg>(w, u)) {
+                uint32_t s_mask = 0, first_mask = 0, last_mask = 0;
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
-                    if (!w.active[t]) continue;
-                    if (!Cfg::SPARSE && t % MW != wi) continue;
-                    const bool do_pv = prev >= 0 && key_in_tile<Cfg>(w, t, prev);
-                    const bool do_s = u >= 0 && key_in_tile<Cfg>(w, t, u);
-                    if (!do_pv && !do_s) continue;
-                    int k;
-                    if constexpr (Cfg::SPARSE) {
-                        k = turn++;
-                        if (t % MW != wi) continue;
-                    } else {
-                        // (the final step of a dense walk is u_hi + 1)
-                        k = item_base + blocks_before(w, t, u >= 0 ? u : prev + 1);
-                    }
-                    if (do_pv && !warp_wait(&bars->p_full[t], pv_count[t] & 1, abort_flag, p, SITE_MMA_P)) {
-                        ok = false;
-                        break;
-                    }
-                    if (MW > 1 && !wait_turn(issued, k, abort_flag, p, SITE_TURN)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        if (do_pv) {
-                            issue_pv<Cfg>(tmem + Cfg::O_COL0 + t * D, tmem + t * Cfg::S_COL, vdesc, !first_pv[t]);
-                            if (prev == w.last[t]) mma_commit(&bars->o_full[t]);
-                        }
-                        if (do_s) {
-                            issue_qk<Cfg>(tmem + t * Cfg::S_COL, qdesc[t], kdesc);
-                            mma_commit(&bars->s_full[t]);
-                            // Q_t is free for the next item once its last S MMA is done.
-                            if (u == w.last[t]) mma_commit(&bars->q_empty[t]);
-                        }
-                        if (MW > 1) {
-                            __threadfence_block();
-                            *issued = k + 1;
-                        }
-                    }
-                    __syncwarp();
-                    issued_any = true;
-                    if (do_pv) {
-                        first_pv[t] = false;
-                        ++pv_count[t];
-                    }
+                    if (w.active[t] && key_in_tile<Cfg>(w, t, u)) s_mask |= 1u << t;
+                    if (u == w.first[t]) first_mask |= 1u << t;
+                    if (u == w.last[t]) last_mask |= 1u << t;
                 }
-                if (!ok) break;
-                // This issuer is done with the stage once its MMAs of the step are.
-                if (elect_one()) {
-                    if (issued_any) mma_commit(&bars->ring_empty[stage]);
-                    else mbar_arrive(&bars->ring_empty[stage]);
-                }
-                __syncwarp();
+                ok = mma_step(s_mask, first_mask, last_mask);
+                any_step = true;
             }
-            item_base += item_blocks(w);
         }
+        // Final step: the last P V of each tile.
+        if (ok && any_step) ok = mma_step(0u, 0u, 0u);
         // Every MMA this warp issued has finished before teardown.
         if (elect_one()) {
             mma_commit(&bars->drain[wi]);
@@ -767,10 +780,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 mx0 = fmax3(mx0, mx1, __uint_as_float(sr[BN - 4]));
                 mx2 = fmax3(mx2, mx3, __uint_as_float(sr[BN - 3]));
                 const float mx = fmax3(mx0, mx2, fmaxf(__uint_as_float(sr[BN - 2]), __uint_as_float(sr[BN - 1])));
-                // Reference maximum.  It moves only when the row maximum grows by
-                // more than kRescaleLog2 (bf16 path: P stays below 2^8, exact
-                // since O and l share the reference); the FP8 path tracks it
-                // exactly so that P <= 1 before the e4m3 scaling.
+                // Reference maximum m.  It moves only when the row maximum
+                // exceeds it by more than RESCALE_LOG2 (so P <= 2^RESCALE_LOG2;
+                // exact, since O and l share the reference), and then to the
+                // row maximum plus RESCALE_HEADROOM.
                 const float m_tile = mx * mult;
                 float m_new = m;
                 if (m_tile > m + Cfg::RESCALE_LOG2 || m == -INFINITY)
@@ -886,31 +899,73 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             if (!ok) break;
             tc_fence_after();
-                // l = 0 only for a row that sees no key: O = 0, LSE = -inf.
-                float out_mult = l > 0.0f ? 1.0f / l : 0.0f;
-                if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / Cfg::P8_SCALE);
+            // l = 0 only for a row that sees no key: O = 0, LSE = -inf.
+            float out_mult = l > 0.0f ? 1.0f / l : 0.0f;
+            if constexpr (Cfg::FP8) out_mult *= vmax * (1.0f / Cfg::P8_SCALE);
+            if constexpr (Cfg::O_VIA_TMA) {
+                // One 64-column box at a time: TMEM -> bf16 in registers -> this
+                // warp's slot (row = lane, 16-byte chunk x at x ^ (lane & 7)) ->
+                // TMA store of rows [row0, row0 + 32).  The conversion of a box
+                // overlaps the store of the previous one reading the slot.
+                const int row0 = qs + quad * 32;
+                // (the slots sit right below the barriers: no extra live pointer)
+                uint8_t* slot = reinterpret_cast<uint8_t*>(bars) - Cfg::EPI_BYTES + warp * Cfg::EPI_SLOT_BYTES;
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb) {
+                    uint32_t orr[64];
+                    tmem_ld32(o_tmem + cb * 64, orr);
+                    tmem_ld32(o_tmem + cb * 64 + 32, orr + 32);
+                    tmem_wait_ld();
+                    reg_fence32(orr);
+                    reg_fence32(orr + 32);
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int x = 0; x < 32; ++x)
+                        pk[x] = pack_bf16x2(__uint_as_float(orr[2 * x]) * out_mult,
+                                            __uint_as_float(orr[2 * x + 1]) * out_mult);
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int x = 0; x < 8; ++x)
+                        *reinterpret_cast<uint4*>(slot + lane * 128 + ((x ^ (lane & 7)) << 4)) =
+                            make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.N) {
+                        tma_store_4d(&tmap_o, slot, cb * 64, h, row0, b);
+                        bulk_commit_group();
+                    }
+                }
+            } else {
                 const bool store = i < p.N;
                 __nv_bfloat16* orow =
                     reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * p.N + i) * p.H + h) * D;
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t orr[32];
                     tmem_ld32(o_tmem + c * 32, orr);
                     tmem_wait_ld();
                     reg_fence32(orr);
                     uint32_t pk[16];
-    #pragma unroll
+#pragma unroll
                     for (int x = 0; x < 16; ++x)
                         pk[x] = pack_bf16x2(__uint_as_float(orr[2 * x]) * out_mult,
                                             __uint_as_float(orr[2 * x + 1]) * out_mult);
                     if (store) {
                         uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-    #pragma unroll
+#pragma unroll
                         for (int x = 0; x < 4; ++x)
                             dst[x] = make_uint4(pk[4 * x], pk[4 * x + 1], pk[4 * x + 2], pk[4 * x + 3]);
                     }
                 }
-                if (store) p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.69314718055994530942f;
+            }
+            if (i < p.N) p.lse[static_cast<size_t>(bh) * p.N + i] = (m + __log2f(l)) * 0.69314718055994530942f;
+        }
+        // The output stores have finished reading the slots (and written O)
+        // before the CTA can exit.
+        if constexpr (Cfg::O_VIA_TMA) {
+            if (lane == 0) bulk_wait_group_all();
+            __syncwarp();
         }
     }
 

@@ -7,8 +7,10 @@
 
 namespace attn {
 
+// o: the bf16 output as {d, H, N, B} with a box of {64, 1, 32, 1} and the
+// 128-byte swizzle (one softmax warp's rows, one column box).
 struct FwdMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, o;
 };
 
 // Tile geometry an instantiation needs from the host (tensor-map boxes).
@@ -40,7 +42,7 @@ cudaError_t launch_fwd(const FwdMaps& maps, const FwdParams& p, int max_ctas, cu
     const long long units = static_cast<long long>(p.n_mblocks) * p.B * p.H;
     const long long grid = units < max_ctas ? units : max_ctas;
     kernel<<<dim3(static_cast<unsigned>(grid)), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream>>>(maps.q, maps.k,
-                                                                                              maps.v, p);
+                                                                                              maps.v, maps.o, p);
     return cudaGetLastError();
 }
 
