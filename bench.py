@@ -178,14 +178,16 @@ def cublaslt_fp8_peak():
 # The sources each timed kernel is compiled from: a recorded DRAM traffic
 # figure is used only while these files are unchanged.
 KERNEL_SOURCES = {
-    "attn_fwd": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_bf16_d128.cu"),
-    "attn_fwd_fp8": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d128.cu"),
-    "attn_fwd_fp8_d256": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_fwd_la_kernel.cuh", "attn_launch.cuh",
-                          "fwd_fp8_d256.cu"),
-    "attn_fwd_fp8_d64": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d64.cu"),
+    "attn_fwd": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_bf16_d128.cu"),
+    "attn_fwd_fp8": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_fp8_d128.cu"),
+    "attn_fwd_fp8_d256": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_fwd_kernel.cuh", "attn_fwd_la_kernel.cuh",
+                          "attn_launch.cuh", "fwd_fp8_d256.cu"),
+    "attn_fwd_fp8_d64": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh",
+                         "fwd_fp8_d64.cu"),
     "fp8_prep": ("fp8_prep.cu", "fp8_prep.cuh", "fp8_prep_tc.cu", "sm103_ptx.cuh"),
     "attn_bwd": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_bwd_kernel.cuh", "attn_bwd.cu", "attn_bwd.cuh"),
-    "attn_fwd_sparse": ("sm103_ptx.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh", "fwd_sparse_d128.cu"),
+    "attn_fwd_sparse": ("sm103_ptx.cuh", "sm103_bulk.cuh", "attn_fwd_kernel.cuh", "attn_launch.cuh",
+                        "fwd_sparse_d128.cu"),
 }
 
 
