@@ -519,12 +519,17 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--fp8-peak", action="store_true", help="measure the cuBLASLt e4m3 GEMM peak and exit")
     ap.add_argument("--spec-peak", action="store_true", help="measure the tcgen05 spec dense peak and exit")
+    ap.add_argument("--sweep", choices=["bf16", "fp8", "bwd"],
+                    help="time every point of the 16384-token sweep (one JSON line each) and exit")
     args = ap.parse_args()
     if args.fp8_peak:
         measure_fp8_peak()
         return
     if args.spec_peak:
         measure_spec_peak()
+        return
+    if args.sweep:
+        run_sweep(args.sweep, args.warmup)
         return
     w = workload(args.workload)
     if args.impl == "reference":
@@ -918,6 +923,77 @@ def fp8_secondary(api, device, stream, steps):
         out["frac_of_cublaslt_fp8_gemm"] = round(out["fwd"]["tflops"] / cublaslt_fp8_peak(), 4)
         out["cublaslt_fp8_gemm_tflops"] = cublaslt_fp8_peak()
     return out
+
+
+def run_sweep(kind: str, warmup: int):
+    """Every point of the 16384-token sweep (hidden 2048: B = 16384 / N,
+    H = 2048 / d) for one path, in one process: per point, inputs of
+    B x N x H x d (each tensor 64 MB, larger than L2 together), W untimed
+    launches, then about half a second of launches timed with CUDA events on
+    the launching stream, the SM clock sampled meanwhile."""
+    import torch
+
+    from exact_attention_71_gb300 import api
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    uuid = None
+    try:
+        uuid = subprocess.run(["nvidia-smi", "--query-gpu=uuid", "--format=csv,noheader", "-i", "0"],
+                              capture_output=True, text=True, timeout=30).stdout.strip() or None
+    except Exception:
+        pass
+    peaks, src = load_peaks()
+    dims = (64, 128) if kind == "bwd" else (64, 128, 256)
+    for d in dims:
+        for causal in (False, True):
+            for n in (512, 1024, 2048, 4096, 8192, 16384):
+                prefix = {"bf16": "c3", "fp8": "fp8", "bwd": "bwd"}[kind]
+                key = f"{prefix}:{n}:{d}:{int(causal)}" if kind != "bwd" else f"bwd:{n}:{int(causal)}:{d}"
+                w = workload(key)
+                tensors, _ = make_inputs(w, device, seed=0)
+                q, k, v = tensors[:3]
+                B, H, N = w["B"], w["H"], w["N"]
+                o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=device)
+                lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+                if kind == "bf16":
+                    def fn():
+                        api.attn_fwd(q, k, v, causal=causal, out=o, lse=lse, stream=stream)
+                elif kind == "fp8":
+                    pp = api.fp8_prepare_qkv(q, k, v, api.MODE_BLOCK_HADAMARD, 1234, stream=stream)
+
+                    def fn():
+                        api.attn_fwd_fp8(*pp, causal=causal, out=o, lse=lse, stream=stream)
+                else:
+                    do = tensors[3]
+                    api.attn_fwd(q, k, v, causal=causal, out=o, lse=lse, stream=stream)
+                    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                    work = torch.empty(api.bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=device)
+
+                    def fn():
+                        api.attn_bwd(do, q, k, v, o, lse, causal=causal, dq=dq, dk=dk, dv=dv, workspace=work,
+                                     stream=stream)
+                for _ in range(warmup):
+                    fn()
+                torch.cuda.synchronize(device)
+                probe = time_loop(fn, 3, stream) / 3
+                steps = max(10, min(2000, int(500.0 / max(probe, 1e-3))))
+                with ClockSampler(uuid) as cs:
+                    ms = time_loop(fn, steps, stream) / steps
+                st = api.device_status()
+                if st[0] != 0:
+                    raise SystemExit(f"device status {st} at {key}")
+                flops = flops_per_step(w)
+                tf = flops / (ms / 1e3) / 1e12
+                peak = peaks["bf16_tflops"] * (2.0 if kind == "fp8" else 1.0)
+                sp = spec_peak()
+                sp_tf = (sp or {}).get("e4m3_tflops_spec" if kind == "fp8" else "bf16_tflops_spec")
+                print(json.dumps({"sweep": kind, "workload": key, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                                  "ms": round(ms, 5), "tflops": round(tf, 1), "frac_of_measured_peak": round(tf / peak, 4),
+                                  "frac_of_spec_dense": round(tf / sp_tf, 4) if sp_tf else None, "steps": steps,
+                                  "clocks": cs.summary()}), flush=True)
+                del tensors, q, k, v, o, lse
+                torch.cuda.empty_cache()
 
 
 if __name__ == "__main__":
