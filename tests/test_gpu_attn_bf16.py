@@ -114,6 +114,30 @@ def test_outputs_written_exactly_once_and_nothing_outside():
     assert torch.isnan(ob[B * N * H * d:]).all() and torch.isnan(lb[B * H * N:]).all()
 
 
+@pytest.mark.parametrize("B,H,N,d", [
+    (1, 19, 4096, 64),     # 304 causal items: two whole rounds of 152 CTAs
+    (1, 10, 4096, 128),    # 160: one round and a partial one
+    (2, 100, 256, 64),     # one query block per head
+    (1, 7, 4000, 128),     # fewer items than CTAs, ragged last tile
+    (3, 37, 1792, 128),    # 777: five rounds and 17 items
+    (1, 12, 2048, 256),    # head dim 256 (one 128-row tile per item)
+])
+def test_causal_item_order_covers_every_row(B, H, N, d):
+    """The causal work order (rounds cut out of a head-major sequence, the
+    lightest items last) must hand every (query block, head) to exactly one
+    CTA: NaN-prefilled outputs are all written, and sampled rows of every head
+    match the oracle."""
+    q, k, v = synth.qkv_bf16(B, N, H, d, seed=12)
+    o = torch.full((B, N, H, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    api.attn_fwd(to_dev(q), to_dev(k), to_dev(v), causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+    rows = np.array(sorted({0, 127, 128, 255, N // 2, N - 1} & set(range(N))))
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True, rows=rows)
+    assert_bf16_parity(errors(gpu_rows(o, rows), o_ref, lse_rows(lse, rows), lse_ref), f"order B{B} H{H} N{N} d{d}")
+
+
 def test_repeat_is_bitwise_deterministic():
     q, k, v = (to_dev(t) for t in synth.qkv_bf16(1, 900, 4, 128, seed=7))
     o1, l1 = api.attn_fwd(q, k, v, causal=True)
