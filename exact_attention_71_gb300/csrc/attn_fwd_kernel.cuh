@@ -124,8 +124,8 @@ struct FwdCfg {
     static constexpr float P8_SCALE = FP8 ? 16.0f : 1.0f;
     // FP8: when the reference moves, it is set this far (log2 units) above
     // the new row maximum, so that the next moves need a larger jump (the
-    // outlier workload's maxima grow in jumps); the tile's P are then <= 1/4.
-    static constexpr float RESCALE_HEADROOM = FP8 ? 2.0f : 0.0f;
+    // outlier workload's maxima grow in jumps); the tile's P are then <= 1/8.
+    static constexpr float RESCALE_HEADROOM = FP8 ? 3.0f : 0.0f;
     // Register split: the launch gives every thread LAUNCH_REGS; the load /
     // MMA warpgroup drops to LOW_REGS and the softmax warpgroups rise to
     // HIGH_REGS.  The sum stays within the launch allocation.

@@ -25,11 +25,11 @@ with f16 intermediates.
     place of V.
   * e4m3 subnormals (P_j c_j < 2^-6): the error is absolute, <= 2^-10 in
     P_j c_j, i.e. <= 2^-10 / (c_j l) in the weight p_j, with l the kernel's
-    row sum.  The kernel's reference maximum lies at most 2 (log2 units)
-    above the row's largest score (its rescale headroom), so l >= 2^-2 /
+    row sum.  The kernel's reference maximum lies at most 3 (log2 units)
+    above the row's largest score (its rescale headroom), so l >= 2^-3 /
     p_max (p_max the row's largest weight).  These errors are independent
     and zero-mean, so their sum over the visible keys has a standard
-    deviation <= 2^-10 * 4 * p_max * sqrt(sum_j (V_jc / c_j)^2) / sqrt(3);
+    deviation <= 2^-10 * 8 * p_max * sqrt(sum_j (V_jc / c_j)^2) / sqrt(3);
     the bound allows 7 of them.
   * the bf16 rounding of O, and 2^-12 for the float32 arithmetic.
 The bound is loose for most rows; random rounding errors give a relative RMS
@@ -155,7 +155,7 @@ def _dequant(codes, scales):
 
 FP8_P_REL = 2.0 ** -4 + 2.0 ** -7    # e4m3 round-to-nearest (normal range) + f16 exponential
 FP8_P_SUBNORMAL = 2.0 ** -10          # half the e4m3 subnormal spacing
-FP8_HEADROOM = 4.0                    # 2^2: the kernel's reference lies <= 2 above the row maximum
+FP8_HEADROOM = 8.0                    # 2^3: the kernel's reference lies <= 3 above the row maximum
 FP8_SIGMAS = 7.0
 FP8_REL_RMS = 5e-2
 
