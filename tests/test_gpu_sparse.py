@@ -62,6 +62,24 @@ def test_rows_that_see_no_key():
     assert frac >= 0.5
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_items_per_cta_with_inactive_tiles(d, causal):
+    """640 work items (about four per CTA on a 152-SM part): a CTA's key walk
+    runs on from one item into the next, carrying the last P V of each tile.
+    Random masks, query tiles that see no key block (inactive tiles), and
+    heads that see nothing at all (items with no key step) between active
+    items."""
+    B, N, H = 2, 2048, 40
+    block = _mask(B, H, N, 0.35, seed=40 + d)
+    T = block.shape[2]
+    block[:, :, ::5, :] = 0              # every fifth query tile sees no key
+    block[:, 3::7, :, :] = 0             # every seventh head sees nothing
+    rows = synth.sample_rows(N, 48, seed=8, must=(0, 127, 128, 255, 256, 640, 767, N - 1))
+    frac = _run(B, N, H, d, block, causal=causal, seed=4, rows=rows)
+    assert 0.1 < frac < 0.9
+
+
 def test_all_ones_mask_equals_dense_forward():
     B, N, H, d = 1, 1000, 2, 128
     q, k, v = synth.qkv_bf16(B, N, H, d, seed=6)
