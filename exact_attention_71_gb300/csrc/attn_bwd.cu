@@ -120,6 +120,15 @@ cudaError_t run_bwd_impl(const BwdMaps& maps, const BwdParams& p, const void* o,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     auto kernel = attn_bwd_kernel<Cfg>;
+    if constexpr (Cfg::REG_SPLIT) {
+        // The register split (setmaxnreg) assumes every thread is launched
+        // with exactly LAUNCH_REGS registers; a different count could make the
+        // increase wait forever, so such a build is refused.
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, kernel);
+        if (e != cudaSuccess) return e;
+        if (attr.numRegs != Cfg::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+    }
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kernel<<<static_cast<unsigned>(ctas), Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(maps.q, maps.k, maps.v, maps.dout,

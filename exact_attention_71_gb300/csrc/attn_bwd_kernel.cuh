@@ -22,16 +22,20 @@
 // global memory with one bulk reduction per step (other key tiles add into
 // the same rows).
 //
-// Roles (320 threads):
-//   warps 0-3  elementwise warpgroup: thread = key row; P, dS
-//   warps 4-7  dQ warpgroup: thread = head dimension; dQ^T out of tensor
-//              memory into a staging buffer and a bulk add to global memory;
-//              at the end the dK epilogue (thread = key row)
-//   warp  8    TMA producer: K, V once; per step Q, dO (ring), LSE, D
-//   warp  9    MMA issuer (one elected lane)
-// Tensor memory (512 columns): dV [0, d), dK [d, 2d), S^T double-buffered
-// at 2d and 2d + 64, dP^T at 2d + 128, dQ^T at 2d + 192.  P (bf16 pairs)
-// overwrites the first 32 columns of its S^T buffer.  dS^T goes to shared
+// Roles (448 threads; 512 at d = 64):
+//   warps 0-7   two elementwise warpgroups: thread = key row; P, dS, each
+//               for half of the step's query columns
+//   warps 8-11  dQ warpgroup: thread = head dimension; dQ^T out of tensor
+//               memory into a staging buffer and a bulk add to global
+//               memory; at the end the dK epilogue (thread = key row)
+//   warp  12    TMA producer: K, V once; per step Q, dO (ring), LSE, D
+//   warp  13    MMA issuer (one elected lane)
+//   warps 14-15 (d = 64) idle: they complete the fourth warpgroup, so that
+//               a register split (setmaxnreg) can raise the elementwise
+//               warpgroups above the 128 registers of the launch
+// Tensor memory (512 columns, d = 128): dV [0, d), dK [d, 2d), S^T
+// double-buffered at 2d and 2d + 64, dP^T at 2d + 128, dQ^T at 2d + 192.
+// P (bf16 pairs) overwrites the first columns of its S^T buffer.  dS^T goes to shared
 // memory only (double-buffered), where it serves as the K-major A operand of
 // dK and the MN-major B operand of dQ^T; so dP^T of the next step can be
 // issued as soon as this step's dS is written, ahead of dK and dQ^T, and the
@@ -119,7 +123,16 @@ struct BwdCfg {
     // Two elementwise warpgroups, each owning half of the step's query columns.
     static constexpr int EW_WGS = 2, EW_COLS = BM / EW_WGS;
     static constexpr int EW_WARP0 = 0, DQ_WARP0 = 4 * EW_WGS, LOAD_WARP = DQ_WARP0 + 4, MMA_WARP = LOAD_WARP + 1;
-    static constexpr int THREADS = (MMA_WARP + 1) * 32;
+    // d = 64: two idle warps complete the load / MMA warpgroup (512 threads,
+    // four whole warpgroups), so that a register split can give the
+    // elementwise warpgroups, which keep 64 scores of P per thread, more than
+    // the 128 registers a thread gets at launch.  d = 128 needs no split.
+    static constexpr bool REG_SPLIT = D == 64;
+    static constexpr int THREADS = REG_SPLIT ? 512 : (MMA_WARP + 1) * 32;
+    static constexpr int LAUNCH_REGS = 128;
+    static constexpr int EW_REGS = 152, DQ_REGS = 120, LM_REGS = 88;
+    static_assert(!REG_SPLIT || 2 * 128 * EW_REGS + 128 * DQ_REGS + 128 * LM_REGS <= LAUNCH_REGS * THREADS,
+                  "register split");
     static constexpr int BAR_BYTES = 256;
     // Shared memory (offsets from a 1024-byte aligned base).
     static constexpr int OFF_K = 0;
@@ -284,6 +297,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t tmem = bars->tmem_base;
     const int T = w.steps;
 
+    if (warp >= Cfg::LOAD_WARP) {
+    if constexpr (Cfg::REG_SPLIT) regs_decrease<Cfg::LM_REGS>();
     if (warp == Cfg::LOAD_WARP) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && T > 0) {
@@ -438,7 +453,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             __syncwarp();
         }
+    }
     } else if (warp < Cfg::DQ_WARP0) {
+        if constexpr (Cfg::REG_SPLIT) regs_increase<Cfg::EW_REGS>();
         // ------------------------------------------------------------ elementwise: P, dS
         constexpr int EC = Cfg::EW_COLS;                 // query columns of this warpgroup
         const int g = warp >> 2;                         // warpgroup: columns [g EC, g EC + EC)
@@ -561,6 +578,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
         }
     } else {
+        if constexpr (Cfg::REG_SPLIT) regs_decrease<Cfg::DQ_REGS>();
         // ------------------------------------------------------------ dQ: tensor memory -> bulk add
         const int quad = warp & 3;
         const int r = quad * 32 + lane;                  // dimension (dQ^T) or query (dQ); key row (dK)
