@@ -18,6 +18,45 @@
 #include "attn_launch.cuh"
 #include "fp8_prep.cuh"
 
+#include <algorithm>
+#include <vector>
+
+namespace attn {
+
+bool causal_item_order(int nmb, int BH, int G, ItemOrder* order) {
+    order->n = 0;
+    const long long n = static_cast<long long>(nmb) * BH;
+    if (n <= 0 || n > kOrderMax || G <= 0 || BH > 0xffff || nmb > 0xffff) return false;
+    const int full = static_cast<int>((n / G) * G), rest = static_cast<int>(n) - full;
+    struct It {
+        int mb, bh;
+    };
+    // The `rest` lightest items, (query block ascending, head ascending)
+    // positions below `rest`, form the last round; the rest, head by head
+    // with the query block descending, make up the full rounds.
+    std::vector<It> body, tail;
+    body.reserve(static_cast<size_t>(full));
+    for (int bh = 0; bh < BH; ++bh)
+        for (int mb = nmb - 1; mb >= 0; --mb)
+            if (static_cast<long long>(mb) * BH + bh >= rest) body.push_back({mb, bh});
+    for (int mb = nmb - 1; mb >= 0; --mb)
+        for (int bh = 0; bh < BH; ++bh)
+            if (static_cast<long long>(mb) * BH + bh < rest) tail.push_back({mb, bh});
+    auto heavier = [](const It& a, const It& b) { return a.mb > b.mb; };
+    int k = 0;
+    for (size_t r = 0; r < body.size(); r += static_cast<size_t>(G)) {
+        auto first = body.begin() + static_cast<long>(r);
+        auto last = body.begin() + static_cast<long>(std::min(body.size(), r + static_cast<size_t>(G)));
+        std::stable_sort(first, last, heavier);     // heaviest first; heads ascending among equals
+        for (auto x = first; x != last; ++x) order->e[k++] = static_cast<uint32_t>(x->mb) | (static_cast<uint32_t>(x->bh) << 16);
+    }
+    for (const It& x : tail) order->e[k++] = static_cast<uint32_t>(x.mb) | (static_cast<uint32_t>(x.bh) << 16);
+    order->n = k;
+    return k == n;
+}
+
+}  // namespace attn
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -269,6 +308,15 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
     if ((rc = status_ptr(&p.status)) != ATTN_OK) return rc;
     int sms = 0;
     if ((rc = sm_count(&sms)) != ATTN_OK) return rc;
+    // Causal launches of the two-tile kernels (d = 64, 128) take their work
+    // order from the launch parameters (copied at the launch, so the buffer
+    // is free again when run() returns).
+    static thread_local attn::ItemOrder order;
+    if (causal && !block_mask && d == 128) {
+        const long long units = static_cast<long long>(p.n_mblocks) * B * H;
+        const int G = static_cast<int>(units < sms ? units : sms);
+        if (attn::causal_item_order(p.n_mblocks, B * H, G, &order)) maps.order = &order;
+    }
     cudaError_t e = run(maps, p, sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return cuda_fail(e, block_mask ? "attn_fwd_sparse launch" : (fp8 ? "attn_fwd_fp8 launch" : "attn_fwd launch"));

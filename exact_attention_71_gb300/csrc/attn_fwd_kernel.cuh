@@ -38,6 +38,7 @@
 
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "sm103_bulk.cuh"
 #include "sm103_ptx.cuh"
@@ -257,6 +258,26 @@ __device__ __forceinline__ int round_item(int m) {
     return m * G + ((m & 1) ? (G - 1 - c) : c);
 }
 
+// A causal launch's work order, computed on the host (causal_item_order): the n
+// mod G lightest items (query block ascending, then head) form the last,
+// partial round; the others, taken head by head (query block descending
+// within a head), are cut into rounds of G, each numbered heaviest query
+// block first, then by head.  The zigzag still balances (every round is
+// numbered heaviest first), and a round touches the K and V of about
+// G / n_mblocks heads instead of all of them.  e[item] = query block |
+// (batch*head) << 16.  n = 0: the closed-form order of item_coords.  It rides
+// in the launch's parameters (no memory shared between launches).
+constexpr int kOrderMax = 1024;
+struct ItemOrder {
+    int n;
+    uint32_t e[kOrderMax];
+};
+// The parameter of a kernel built without an order table (4 bytes instead of
+// 4 KB: the other launches do not pay for the table).
+struct NoOrder {
+    int n;
+};
+
 __device__ __forceinline__ void item_coords(const FwdParams& p, int item, int& mb, int& bh) {
     const int BH = p.B * p.H;
     if (p.causal) {
@@ -336,11 +357,18 @@ __device__ __forceinline__ int next_in(const TileKeys& k, int u) {
     }
 }
 
-template <class Cfg>
-__device__ __forceinline__ WorkItem<Cfg::NQ> decode_item(const FwdParams& p, int item) {
+template <class Cfg, class Order = NoOrder>
+__device__ __forceinline__ WorkItem<Cfg::NQ> decode_item(const FwdParams& p, int item,
+                                                        const Order* order = nullptr) {
     WorkItem<Cfg::NQ> w;
     int mb;
-    item_coords(p, item, mb, w.bh);
+    if constexpr (std::is_same<Order, ItemOrder>::value) {
+        const uint32_t e = order->e[item];
+        mb = static_cast<int>(e & 0xffffu);
+        w.bh = static_cast<int>(e >> 16);
+    } else {
+        item_coords(p, item, mb, w.bh);
+    }
     w.b = w.bh / p.H;
     w.h = w.bh % p.H;
     w.q0 = mb * Cfg::NQ * Cfg::BM;
@@ -444,11 +472,14 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
     }
 }
 
-template <class Cfg>
+// ORDERED: the causal work order comes from `order` (a causal launch with a
+// host-built table); otherwise from item_coords.
+template <class Cfg, bool ORDERED = false>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
-                    const FwdParams p) {
+                    const FwdParams p,
+                    const __grid_constant__ typename std::conditional<ORDERED, ItemOrder, NoOrder>::type order) {
     constexpr int D = Cfg::D, BN = Cfg::BN, NQ = Cfg::NQ, BM = Cfg::BM, NSTAGE = Cfg::NSTAGE;
 
     extern __shared__ uint8_t smem_raw[];
@@ -538,7 +569,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
                 const int item = round_item(rnd);
                 if (item >= total_items) continue;
-                const WorkItem<NQ> w = decode_item<Cfg>(p, item);
+                const WorkItem<NQ> w = decode_item<Cfg>(p, item, &order);
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) {
                     if (!w.active[t] || !ok) continue;
@@ -662,7 +693,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
             const int item = round_item(rnd);
             if (item >= total_items) continue;
-            const WorkItem<NQ> w = decode_item<Cfg>(p, item);
+            const WorkItem<NQ> w = decode_item<Cfg>(p, item, &order);
 #pragma unroll
             for (int t = 0; t < NQ; ++t) {
                 if (t % MW == wi && w.active[t] && ok) {
@@ -707,7 +738,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int rnd = 0; rnd * static_cast<int>(gridDim.x) < total_items && ok; ++rnd) {
             const int item = round_item(rnd);
             if (item >= total_items) continue;
-            const WorkItem<NQ> w = decode_item<Cfg>(p, item);
+            const WorkItem<NQ> w = decode_item<Cfg>(p, item, &order);
             const TileKeys tk = tile_keys<Cfg>(w, t);
             const int bh = w.bh, b = w.b, h = w.h;
             const int qs = w.q0 + t * BM;
