@@ -267,13 +267,13 @@ __device__ __forceinline__ int round_item(int m) {
 // G / n_mblocks heads instead of all of them.  e[item] = query block |
 // (batch*head) << 16.  n = 0: the closed-form order of item_coords.  It rides
 // in the launch's parameters (no memory shared between launches).
-constexpr int kOrderMax = 1024;
+constexpr int kOrderMax = 2048;
 struct ItemOrder {
     int n;
     uint32_t e[kOrderMax];
 };
 // The parameter of a kernel built without an order table (4 bytes instead of
-// 4 KB: the other launches do not pay for the table).
+// 8 KB: the other launches do not pay for the table).
 struct NoOrder {
     int n;
 };
