@@ -308,11 +308,13 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
     if ((rc = status_ptr(&p.status)) != ATTN_OK) return rc;
     int sms = 0;
     if ((rc = sm_count(&sms)) != ATTN_OK) return rc;
-    // Causal launches of the two-tile kernels (d = 64, 128) take their work
-    // order from the launch parameters (copied at the launch, so the buffer
-    // is free again when run() returns).
+    // Causal launches of the d = 128 kernels without grouped heads take their
+    // work order from the launch parameters (copied at the launch, so the
+    // buffer is free again when run() returns).  With grouped heads several
+    // query heads already share each K/V head; the order then only crowds
+    // more CTAs onto the same tiles.
     static thread_local attn::ItemOrder order;
-    if (causal && !block_mask && d == 128) {
+    if (causal && !block_mask && d == 128 && Hkv == H) {
         const long long units = static_cast<long long>(p.n_mblocks) * B * H;
         const int G = static_cast<int>(units < sms ? units : sms);
         if (attn::causal_item_order(p.n_mblocks, B * H, G, &order)) maps.order = &order;
