@@ -86,6 +86,8 @@ def library() -> ctypes.CDLL:
         L.attn_set_wait_limit.restype = i
         L.attn_last_error_string.argtypes = []
         L.attn_last_error_string.restype = ctypes.c_char_p
+        L.attn_fwd_work_order.argtypes = [i, i, i, P, i]
+        L.attn_fwd_work_order.restype = i
         _lib = L
         return _lib
 
@@ -491,6 +493,18 @@ def device_status(stream=None):
     site = ctypes.c_int(0)
     rc = library().attn_device_status(ctypes.c_void_p(_stream(stream)), ctypes.byref(site))
     return rc, site.value
+
+
+def fwd_work_order(n_mblocks: int, bh: int, grid: int):
+    """The causal d=128 forward's work order (host only): a list of
+    (query block, batch*head) per item, or None where the launch uses the
+    closed-form order."""
+    n = n_mblocks * bh
+    buf = (ctypes.c_uint * max(n, 1))()
+    got = library().attn_fwd_work_order(n_mblocks, bh, grid, ctypes.cast(buf, ctypes.c_void_p), n)
+    if got == 0:
+        return None
+    return [(buf[k] & 0xFFFF, buf[k] >> 16) for k in range(got)]
 
 
 def default_scale(d: int) -> float:

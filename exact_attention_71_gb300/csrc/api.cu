@@ -329,6 +329,14 @@ int launch_forward(bool fp8, const void* q, const void* k, const void* v, void* 
 
 extern "C" {
 
+int attn_fwd_work_order(int n_mblocks, int BH, int grid, unsigned int* out, int capacity) {
+    if (out == nullptr || n_mblocks <= 0 || BH <= 0 || grid <= 0) return 0;
+    static thread_local attn::ItemOrder order;
+    if (!attn::causal_item_order(n_mblocks, BH, grid, &order) || order.n > capacity) return 0;
+    for (int i = 0; i < order.n; ++i) out[i] = order.e[i];
+    return order.n;
+}
+
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
              int causal, float scale, int window, void* stream) {
     return attn_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, window, stream);

@@ -352,6 +352,28 @@ int attn_device_status(void* stream, int* site);
  */
 int attn_set_wait_limit(unsigned long long cycles);
 
+/*
+ * attn_fwd_work_order -- the order in which a causal forward at head_dim
+ * 128 without grouped heads (H_kv = H, no block mask) hands its work items
+ * to the grid; host code only, no GPU needed (inspection and testing).  A
+ * work item is one batch*head and one query block of 256 rows.  The grid
+ * takes the items in rounds of `grid`: round m goes to the CTAs in order
+ * when m is even and in reverse when odd.  The order: the n mod grid
+ * lightest items (query block ascending, then head) form the last, partial
+ * round; the others, taken head by head (query block descending within a
+ * head), are cut into rounds of `grid`, each numbered heaviest query block
+ * first, then by head.
+ *   n_mblocks : query blocks per head, ceil(N / 256)
+ *   BH        : B * H
+ *   grid      : CTAs of the launch, min(n_mblocks * BH, SM count)
+ *   out       : HOST array of `capacity` entries; entry i = query block of
+ *               item i | (its batch*head) << 16
+ * Returns the number of entries written (n_mblocks * BH), or 0 when such a
+ * launch uses the closed-form order instead (more than 2048 items), when
+ * `capacity` is too small, or for invalid sizes.
+ */
+int attn_fwd_work_order(int n_mblocks, int BH, int grid, unsigned int* out, int capacity);
+
 /* Text of the last error of the calling thread ("" if none). */
 const char* attn_last_error_string(void);
 

@@ -212,3 +212,39 @@ def test_host_bindings_check_their_arguments(lib):
         api.attn_bwd_host(q[:, :8], q, k, k, q, torch.zeros(2, 4, 16))     # dout shaped unlike q
     with pytest.raises(ValueError):
         api.attn_bwd_host(q, q, k, k, q, torch.zeros(2, 4, 16), dk=torch.zeros(2, 16, 4, 64, dtype=torch.bfloat16))
+
+
+@pytest.mark.parametrize("nmb,bh,grid", [(16, 64, 152), (64, 16, 152), (16, 19, 152), (1, 200, 152),
+                                          (7, 111, 152), (16, 128, 152), (3, 5, 7), (32, 64, 152)])
+def test_causal_work_order(lib, nmb, bh, grid):
+    """The causal forward's host-built work order: a permutation of the
+    items; every full round numbered heaviest query block first; the last,
+    partial round holds the lightest items; the zigzag over rounds balances
+    the per-CTA work (query block q of a head costs 4q + 3 key blocks of 128);
+    and a full round touches few heads."""
+    order = api.fwd_work_order(nmb, bh, grid)
+    n = nmb * bh
+    assert order is not None and len(order) == n
+    assert sorted(order) == sorted((m, h) for h in range(bh) for m in range(nmb))
+    full = n // grid * grid
+    per_head = nmb - -(-(n - full) // bh)           # fewest items a head keeps outside the last round
+    for r in range(0, full, grid):
+        mbs = [m for m, _ in order[r:r + grid]]
+        assert mbs == sorted(mbs, reverse=True)
+        heads = {h for _, h in order[r:r + grid]}
+        assert len(heads) <= -(-grid // max(per_head, 1)) + 1
+    tail = order[full:]
+    if tail and full:
+        assert max((m, h) for m, h in tail) < min((m, h) for m, h in order[:full])
+    load = [0] * grid
+    for i, (m, _) in enumerate(order):
+        rnd, c = divmod(i, grid)
+        load[c if rnd % 2 == 0 else grid - 1 - c] += 4 * m + 3
+    # No CTA's work exceeds the mean by a whole heaviest item (items are
+    # indivisible; 3-7 % above the mean for the larger shapes here).
+    assert max(load) - sum(load) / grid <= 4 * (nmb - 1) + 3
+
+
+def test_causal_work_order_beyond_the_table(lib):
+    assert api.fwd_work_order(64, 40, 152) is None      # 2560 items: the closed-form order
+    assert lib.attn_fwd_work_order(4, 4, 4, None, 16) == 0
