@@ -131,7 +131,7 @@ struct FwdCfg {
     // MMA warpgroup drops to LOW_REGS and the softmax warpgroups rise to
     // HIGH_REGS.  The sum stays within the launch allocation.
     static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8 > 255 ? 248 : (65536 / THREADS) / 8 * 8;
-    static constexpr int LOW_REGS = FP8 ? 72 : 112;
+    static constexpr int LOW_REGS = FP8 ? 72 : 104;
     static constexpr int HIGH_REGS_RAW = ((LAUNCH_REGS * THREADS - LOW_REGS * 128) / (NQ * 128)) / 8 * 8;
     static constexpr int HIGH_REGS = HIGH_REGS_RAW > 248 ? 248 : HIGH_REGS_RAW;
     static_assert(HIGH_REGS * NQ * 128 + LOW_REGS * 128 <= LAUNCH_REGS * THREADS, "register split");
